@@ -1,0 +1,420 @@
+"""Benchmark of the tiled tcgen05 GEMM (libtilegemm) on one GB300.
+
+Headline: fp16 GEMM C = A.B, M = N = K = 4096, row-major, entries uniform[-1,1]
+from seed 1002, fp32 accumulation, fp16 output; TFLOP/s = 2 M N K / kernel
+time.  One step = one tg_gemm call.  The 96 MB working set is smaller than
+L2, so a 512 MB buffer is written between timed steps (outside the timed
+window) and every step starts cold.  Further lines in "workloads": the bf16
+variant, the fused-epilogue GEMM (8192 x 8192 x 4096, relu(scale*AB+bias)+R)
+beside the same shape without epilogue, the ragged/strided fp16 problem and
+the skinny bf16 problems (the last one reported in GB/s against HBM).
+
+--impl reference times the CPU oracle (fp64, all host cores) on a bounded
+sample of rows of the headline workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "fp16 GEMM 4096x4096x4096 row-major, fp32 accumulate, fp16 out"
+METRIC = "GEMM TFLOP/s (fp16, fp32 acc) at 4096^3"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "tiled_gemm_layouts_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        e = d.get(workload_key)
+        if e and e.get("kernel_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                "sw_power_cap"), parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def workload_specs():
+    """Synthetic workloads (seed = 1000 + index, draws in the order A, B, bias, scale, R)."""
+    import synthetic as S
+    return {
+        "fp16_4096": dict(M=4096, N=4096, K=4096, dtype=S.F16, seed=1002),
+        "bf16_4096": dict(M=4096, N=4096, K=4096, dtype=S.BF16, seed=1002),
+        "fp16_8192x8192x4096_fused": dict(M=8192, N=8192, K=4096, dtype=S.F16, seed=1003,
+                                          bias=True, scale=True, residual=True, relu=True),
+        "fp16_8192x8192x4096_plain": dict(M=8192, N=8192, K=4096, dtype=S.F16, seed=1003),
+        "fp16_4000x3000x1000_strided": dict(M=4000, N=3000, K=1000, dtype=S.F16, seed=1004,
+                                            permA=1, ldb=3064, dist="normal", bias=True),
+        "bf16_16384x1024x8192_scale": dict(M=16384, N=1024, K=8192, dtype=S.BF16, seed=1005,
+                                           scale=True),
+        "bf16_32x16384x16384_scale": dict(M=32, N=16384, K=16384, dtype=S.BF16, seed=1005,
+                                          scale=True),
+    }
+
+
+def make_problem(spec):
+    import synthetic as S
+    kw = dict(spec)
+    relu = kw.pop("relu", False)
+    M, N, K, dtype, seed = (kw.pop(k) for k in ("M", "N", "K", "dtype", "seed"))
+    p = S.gemm_problem(M, N, K, dtype, seed, **kw)
+    p["relu"] = relu
+    return p
+
+
+def algorithmic_bytes(p) -> int:
+    M, N, K = p["M"], p["N"], p["K"]
+    b = 2 * (M * K + K * N + M * N)
+    if p.get("bias") is not None:
+        b += 2 * N
+    if p.get("scale") is not None:
+        b += 2 * M
+    if p.get("R") is not None:
+        b += 2 * M * N
+    return b
+
+
+class DeviceProblem:
+    def __init__(self, tg, p):
+        import numpy as np
+        import torch
+        self.p = p
+        self.tg = tg
+        dev = lambda a: None if a is None else torch.from_numpy(
+            np.ascontiguousarray(a).view(np.int16)).cuda()
+        self.A, self.B = dev(p["A"]), dev(p["B"])
+        self.bias, self.scale, self.R = dev(p.get("bias")), dev(p.get("scale")), dev(p.get("R"))
+        self.C = torch.empty((p["M"], p["N"]), dtype=torch.int16, device="cuda")
+        self.epi = tg.make_epilogue(self.bias, self.scale, p.get("relu", False), self.R,
+                                    p.get("ldr", 0) or 0)
+
+    def call(self, stream):
+        p = self.p
+        self.tg.gemm(p["M"], p["N"], p["K"], self.A, p["lda"], p["permA"], self.B, p["ldb"],
+                     p["permB"], self.C, p["N"], p["dtype"], self.epi, stream)
+
+
+def time_kernel(fn, steps, warmup, flush_buf, stream):
+    """Per-step kernel times (ms) by CUDA events on the launching stream, L2
+    flushed before every step outside the event window."""
+    import torch
+    for _ in range(warmup):
+        flush_buf.fill_(1)
+        fn(stream)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush_buf.fill_(i & 0x7F)
+            starts[i].record(stream)
+            fn(stream)
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def oracle_sample_tflops(p, seconds: float, max_rows: int | None = None):
+    """The oracle as it stands on the first rows of the workload, in chunks of
+    16 rows until `seconds` have passed.  Returns (TFLOP/s, rows, seconds, threads)."""
+    import oracle
+    rows, t0 = 0, time.perf_counter()
+    limit = p["M"] if max_rows is None else min(p["M"], max_rows)
+    while rows < limit and time.perf_counter() - t0 < seconds:
+        r1 = min(limit, rows + 16)
+        oracle.gemm(p, rows=(rows, r1))
+        rows = r1
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * p["N"] * p["K"] / dt / 1e12, rows, dt, oracle.max_threads()
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    p = make_problem(workload_specs()["fp16_4096"])
+    rows_per_step = 32
+    for _ in range(args.warmup):
+        oracle.gemm(p, rows=(0, rows_per_step))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        r0 = (i * rows_per_step) % p["M"]
+        oracle.gemm(p, rows=(r0, r0 + rows_per_step))
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows_per_step * p["N"] * p["K"] * args.steps
+    v = flops / dt / 1e12
+    cores = oracle.max_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (SplitMix64 seed 1002, uniform[-1,1] rounded to fp16)",
+        "config": {"workload": HEADLINE, "sample": f"{rows_per_step} rows of C per step"},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_per_step} of 4096 output rows per step, all K"},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the other workloads and the CPU baseline (for profiling)")
+    ap.add_argument("--workload", default="fp16_4096", help="headline workload key")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_tg_build", os.path.join(ROOT, "tiled_gemm_layouts_gb300", "build.py"))
+    bmod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bmod)
+    bmod.build()
+    import tiled_gemm_layouts_gb300 as tg
+
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    peaks, peak_src = load_peaks()
+    specs = workload_specs()
+
+    # ---------------- headline: device-resident inputs
+    hp = make_problem(specs[args.workload])
+    prob = DeviceProblem(tg, hp)
+    M, N, K = hp["M"], hp["N"], hp["K"]
+    flops = 2.0 * M * N * K
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        times = time_kernel(prob.call, args.steps, args.warmup, flush, stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - t_wall0
+    st, code = tg.tg_debug_status()
+    if st != tg.TG_OK:
+        raise RuntimeError(f"device watchdog fired during the bench: {code:#x}")
+    total_ms = max_over_ranks(sum(times), world)
+    ms = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", 1900.0))  # dense fp16 rate equals bf16's
+    achieved = flops / (statistics.mean(times) * 1e-3) / 1e12
+    traffic = profiled_traffic(args.workload)
+
+    # ---------------- end to end through the public API with host buffers
+    import numpy as np
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
+    hA, hB = pin(hp["A"]), pin(hp["B"])
+    hC = torch.empty((M, N), dtype=torch.int16).pin_memory()
+    dA, dB = torch.empty_like(prob.A), torch.empty_like(prob.B)
+    dC = torch.empty_like(prob.C)
+
+    def e2e_step(s):
+        with torch.cuda.stream(s):
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            tg.gemm(M, N, K, dA, hp["lda"], hp["permA"], dB, hp["ldb"], hp["permB"], dC, N,
+                    hp["dtype"], None, s)
+            hC.copy_(dC, non_blocking=True)
+
+    e2e_times = time_kernel(e2e_step, max(5, args.steps // 2), 3, flush, stream)
+    e2e_ms = max_over_ranks(statistics.mean(e2e_times), world)
+    h2d = 2 * (hA.numel() + hB.numel())
+    d2h = 2 * hC.numel()
+    if not np.array_equal(hC.numpy(), prob.C.cpu().numpy()):
+        raise RuntimeError("end-to-end result differs from the device-resident run")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
+        "data": "synthetic (SplitMix64 seed 1002, uniform[-1,1] rounded to fp16)",
+        "config": {"workload": HEADLINE, "M": M, "N": N, "K": K, "layout": "row-major A, B, C",
+                   "accumulate": "fp32", "l2": "flushed before every step (512 MB write)",
+                   "tile": tg.tg_query_config(M, N, K, hp["dtype"], hp["permA"], hp["permB"]),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_dense_peak": 100.0 * achieved / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops (burst; dense fp16 rate = bf16 rate)",
+                     "kernel_ms_mean": statistics.mean(times),
+                     "kernel_ms_min": min(times), "kernel_ms_max": max(times)},
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+        "gpu": torch.cuda.get_device_name(local),
+    }
+
+    # ---------------- other workloads (rank 0 reports; each replica runs them)
+    if not args.headline_only:
+        others = {}
+        for key in ("bf16_4096", "fp16_8192x8192x4096_plain", "fp16_8192x8192x4096_fused",
+                    "fp16_4000x3000x1000_strided", "bf16_16384x1024x8192_scale",
+                    "bf16_32x16384x16384_scale"):
+            p = make_problem(specs[key])
+            dp = DeviceProblem(tg, p)
+            ts = time_kernel(dp.call, 10, 3, flush, stream)
+            t = statistics.median(ts) * 1e-3
+            f = 2.0 * p["M"] * p["N"] * p["K"]
+            entry = {"tflops": f / t / 1e12, "pct_dense_peak": 100 * f / t / 1e12 / peak,
+                     "ms_median": t * 1e3,
+                     "tile": tg.tg_query_config(p["M"], p["N"], p["K"], p["dtype"], p["permA"],
+                                                p["permB"], dp.epi)}
+            if key.startswith("bf16_32x"):
+                gbs = algorithmic_bytes(p) / t / 1e9
+                entry.update({"gbs": gbs, "hbm_frac": gbs / float(peaks.get("hbm_gbs", 6800.0))})
+            others[key] = entry
+            del dp
+        fused, plain = others["fp16_8192x8192x4096_fused"], others["fp16_8192x8192x4096_plain"]
+        others["fused_over_plain_time"] = fused["ms_median"] / plain["ms_median"]
+        line["workloads"] = others
+        if rank == 0:
+            tfl, rows, secs, cores = oracle_sample_tflops(hp, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": tfl, "unit": "TFLOP/s", "cores": cores,
+                                    "kind": "oracle",
+                                    "sample": f"first {rows} of {M} output rows of the headline "
+                                              f"workload, all K ({secs:.1f} s)"}
+    st, code = tg.tg_debug_status()
+    if st != tg.TG_OK:
+        raise RuntimeError(f"device watchdog fired during the bench: {code:#x}")
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

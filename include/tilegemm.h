@@ -1,0 +1,236 @@
+/*
+ * tilegemm.h -- C ABI of libtilegemm, a tiled GEMM with a fused output-domain
+ * epilogue for GB300 (sm_103a), and its GF(2) layout module.
+ *
+ * Every call takes plain pointers and sizes.  GEMM operand pointers are DEVICE
+ * pointers (memory of the current CUDA device); layout calls are host-only.
+ *
+ * Status codes: every call returns TG_OK (0) or one of the TG_ERR_* codes
+ * below; tg_status_string() names them.  Argument checks run before any
+ * device work, cannot be switched off, and "cannot prove it is safe" is an
+ * error (ninetoothed.org "Named layouts", section "Runtime and compilation":
+ * positive sizes and strides, non-contiguous inputs allowed, output storage
+ * disjoint from every input, checks before kernel work).
+ */
+#ifndef TILEGEMM_H
+#define TILEGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    TG_OK = 0,
+    TG_ERR_INVALID_ARG = 1,        /* null pointer, size <= 0 or > 2^31-1, bad enum, relu not 0/1 */
+    TG_ERR_STRIDE = 2,             /* leading dimension < row width (or <= 0) */
+    TG_ERR_ALIGN = 3,              /* pointer not 16-byte aligned, or ld*2 bytes not a multiple of 16 */
+    TG_ERR_OVERLAP = 4,            /* output bytes intersect an input's bytes */
+    TG_ERR_DTYPE = 5,              /* dtype not TG_F16 / TG_BF16 */
+    TG_ERR_UNSUPPORTED_DEVICE = 6, /* no CUDA device, or not compute capability 10.x with tcgen05 */
+    TG_ERR_CUDA = 7,               /* a CUDA runtime/driver call or the launch failed */
+    TG_ERR_TIMEOUT = 8,            /* a bounded device wait expired (reported by tg_debug_status) */
+    TG_ERR_POINTER = 9,            /* a pointer is not device memory of the current device, or the
+                                      bytes the call touches run past the end of its allocation */
+    TG_ERR_LAYOUT = 10,            /* layout arguments violate a layout invariant */
+    TG_ERR_BUFFER = 11             /* caller's output buffer too small */
+};
+
+typedef enum { TG_F16 = 0, TG_BF16 = 1 } tg_dtype;
+
+/* Explicit permute of an operand's storage.  A transposed input must say so;
+ * a matching size never stands in for a transpose (ninetoothed.org "Named
+ * layouts", section "Contract"). */
+typedef enum { TG_OP_N = 0, TG_OP_T = 1 } tg_perm;
+
+/* Same-output-domain epilogue (ninetoothed.org "Named layouts": a column bias
+ * has axes ("n"), a row scale axes ("m"); bias/ReLU/residual postprocessing):
+ *
+ *     y = acc;  y *= scale_m[m];  y += bias_n[n];  y = max(y, 0);  y += R[m*ldr + n]
+ *
+ * each step only when its operand is given, in that order.  All operands have
+ * the GEMM's dtype and are device pointers; R must not overlap C. */
+typedef struct {
+    const void* bias_n;   /* [N] or NULL */
+    const void* scale_m;  /* [M] or NULL */
+    int relu;             /* 0 or 1 */
+    const void* residual; /* M rows of ldr elements, or NULL */
+    int64_t ldr;          /* residual row stride in elements; 0 means ldc */
+} tg_epilogue;
+
+/*
+ * C = epilogue(A * B), accumulated in fp32, stored as dtype with
+ * round-to-nearest-even.
+ *
+ * The computation is the named-layout GEMM (ninetoothed.org "Named layouts":
+ * acc = zeros(f32); for each of ceil(K/BK) blocks acc += dot(lhs[k], rhs[k]);
+ * output = acc.to(dtype)), tiled over output blocks
+ * (pbelevich.github.io "My Triton From Scratch Part 16: Register Tiles":
+ * several fp32 accumulators per thread, per-element masked stores on edges).
+ *
+ * Layout (strides in elements, inner stride 1, all ld > 0):
+ *   permA = TG_OP_N: A(m,k) = A[m*lda + k], lda >= K   (M x K row-major)
+ *   permA = TG_OP_T: A(m,k) = A[k*lda + m], lda >= M   (storage K x M)
+ *   permB = TG_OP_N: B(k,n) = B[k*ldb + n], ldb >= N   (K x N row-major)
+ *   permB = TG_OP_T: B(k,n) = B[n*ldb + k], ldb >= K   (storage N x K)
+ *   C(m,n) = C[m*ldc + n], ldc >= N.
+ * Requirements: 1 <= M, N, K <= 2^31-1; every pointer 16-byte aligned and
+ * every ld*2 a multiple of 16 bytes (tensor-memory-access copies); C's bytes
+ * disjoint from A, B, bias, scale and R; every pointer inside one device
+ * allocation of the current device that covers all bytes the call touches.
+ *
+ * Ownership: the caller owns all buffers.  The call allocates nothing, makes
+ * one kernel launch on `stream` (0 = legacy default stream) and returns
+ * without synchronising.  `epi` may be NULL (plain GEMM).
+ * Errors: any failed check returns its code before device work starts;
+ * TG_ERR_CUDA if the launch fails.  Device-side watchdog expiries are
+ * reported later by tg_debug_status().
+ */
+int tg_gemm(int64_t M, int64_t N, int64_t K,
+            const void* A, int64_t lda, tg_perm permA,
+            const void* B, int64_t ldb, tg_perm permB,
+            void* C, int64_t ldc, tg_dtype dtype,
+            const tg_epilogue* epi, cudaStream_t stream);
+
+/* Static name of a status code ("TG_OK", "TG_ERR_ALIGN", ...). */
+const char* tg_status_string(int status);
+
+/*
+ * Writes the configuration tg_gemm would use for these arguments into buf
+ * (NUL-terminated, e.g. "swap=0 bm=128 bn=256 pair=0 stages=4 group_m=8
+ * grid=152 tiles=512"); the selector is deterministic (pbelevich.github.io
+ * Part 16, "Choosing the physical thread shape": a deterministic policy, not
+ * an autotuner; ninetoothed.org "Named layouts": tile sizes belong to the
+ * layout).  Needs a device for the SM count; pointers are not inspected.
+ * Environment TG_FORCE_CONFIG="bn=128,swap=0,pair=0,group_m=8" overrides it.
+ * Returns TG_ERR_BUFFER if len is too small.
+ */
+int tg_query_config(int64_t M, int64_t N, int64_t K, tg_dtype dtype, tg_perm permA,
+                    tg_perm permB, const tg_epilogue* epi, char* buf, size_t len);
+
+/*
+ * Reads and clears the device status word of the current device: TG_OK, or
+ * TG_ERR_TIMEOUT if some earlier kernel's bounded wait expired (the kernel
+ * then stopped early and its output is incomplete).  Synchronises the device.
+ * If detail != NULL it receives the raw device code (which wait gave up).
+ */
+int tg_debug_status(int* detail);
+
+/*
+ * Watchdog settings for later launches on this process: the wait limit in
+ * SM clock cycles (0 restores the default of 4e9, about two seconds) and a
+ * test hook: the producer skips arming k-block `skip_kblock` (counted across
+ * the CTA's tiles; -1 = off) so a wait provably expires.
+ */
+int tg_debug_configure(int64_t timeout_cycles, int64_t skip_kblock);
+
+/* ------------------------------------------------------------------------
+ * GF(2) linear layouts (retepy.com "Triton LinearLayout").
+ *
+ * A layout maps named input dims (e.g. register, lane, warp) to named output
+ * dims (e.g. tensor dims) and is linear over GF(2): L(x XOR y) = L(x) XOR
+ * L(y), L(0) = 0, every dim size a power of two (section "Linear Layout").
+ * It is stored as one basis vector per input bit with one coordinate per
+ * output dim (section "Basis-vector representation").  Input tuples and
+ * outputs are passed in the layout's dim order.  Handles are host objects,
+ * owned by the caller, freed with tg_layout_destroy; the library never
+ * retains caller pointers.  Dim names are at most 31 characters.
+ * ---------------------------------------------------------------------- */
+typedef struct tg_layout tg_layout;
+
+/* bases: row-major [sum of in_bits][n_out]; basis i of input dim d lives at
+ * row (in_bits[0] + ... + in_bits[d-1] + i).  Coordinates must fit out_bits.
+ * TG_ERR_LAYOUT on duplicate names, bits outside 0..30 or a coordinate too
+ * large (the invariant check of section "Surjectivity, injectivity, and
+ * broadcasts"). */
+int tg_layout_create(int n_in, const char* const* in_names, const int* in_bits,
+                     int n_out, const char* const* out_names, const int* out_bits,
+                     const int32_t* bases, tg_layout** out);
+void tg_layout_destroy(tg_layout* l);
+
+/* Dim counts, names (copied into name[len]) and log2 sizes. */
+int tg_layout_num_dims(const tg_layout* l, int* n_in, int* n_out);
+int tg_layout_in_dim(const tg_layout* l, int i, char* name, size_t len, int* bits);
+int tg_layout_out_dim(const tg_layout* l, int i, char* name, size_t len, int* bits);
+/* Copies the basis table in tg_layout_create's format. */
+int tg_layout_get_bases(const tg_layout* l, int32_t* bases, size_t count);
+
+/* outs[j] = XOR of the bases selected by the set bits of ins (section
+ * "LinearLayout::apply").  Each ins[i] must be < 2^in_bits[i]. */
+int tg_layout_apply(const tg_layout* l, const int32_t* ins, int32_t* outs);
+
+/* outer o inner: outer applied to every basis of inner (section "Combining
+ * layouts").  inner's out dims must equal outer's in dims (names and sizes,
+ * same order). */
+int tg_layout_compose(const tg_layout* inner, const tg_layout* outer, tg_layout** out);
+
+/* Direct-sum-like product a * b (section "Combining layouts"): dims of b not
+ * in a are appended; for a dim name both have, b's bits become the more
+ * significant bits, i.e. (a*b)(x | y << bits_a) = a(x) | b(y) << outbits_a. */
+int tg_layout_product(const tg_layout* a, const tg_layout* b, tg_layout** out);
+
+/* Restriction to the named input and output dims (section "Combining layouts",
+ * sublayout), in the order given. */
+int tg_layout_sublayout(const tg_layout* l, int n_in, const char* const* in_names,
+                        int n_out, const char* const* out_names, tg_layout** out);
+
+/* Same map with the output dims reordered (transposeOuts). */
+int tg_layout_transpose_outs(const tg_layout* l, int n_out, const char* const* out_names,
+                             tg_layout** out);
+
+/* Rank of the GF(2) matrix by row reduction; injective iff rank = total input
+ * bits, surjective iff rank = total output bits (section "Surjectivity,
+ * injectivity, and broadcasts").  Results in *value. */
+int tg_layout_rank(const tg_layout* l, int* value);
+int tg_layout_is_injective(const tg_layout* l, int* value);
+int tg_layout_is_surjective(const tg_layout* l, int* value);
+
+/* R.invertAndCompose(S) (section "invertAndCompose: derive data movement"):
+ * a layout X from R's input dims to S's input dims with S(X(x)) = R(x) for
+ * every x.  R and S must have the same output dims; S may broadcast (its
+ * pseudoinverse sets free variables to zero).  TG_ERR_LAYOUT if some R(x) is
+ * outside S's image. */
+int tg_layout_invert_and_compose(const tg_layout* R, const tg_layout* S, tg_layout** out);
+
+/* Rank-2 Triton blocked layout -> (register, lane, warp) -> (dim0, dim1)
+ * (section "Blocked-layout example").  Per dim in `order` (minor first):
+ * size_per_thread bits -> register, threads_per_warp -> lane, warps_per_cta
+ * -> warp, then repetitions over the rest of `shape` -> more register bits;
+ * a CTA tile larger than shape broadcasts.  All sizes powers of two. */
+int tg_layout_blocked(const int size_per_thread[2], const int threads_per_warp[2],
+                      const int warps_per_cta[2], const int order[2], const int shape[2],
+                      tg_layout** out);
+
+/* Cooperative traversal of a rank-2 tile by `threads` threads
+ * (pbelevich.github.io Part 12, "Cooperative tile layouts": thread t at
+ * iteration i visits linear index t + i*threads, peeled axis by axis in
+ * `order`) -> (thread, iteration) -> (dim0, dim1).  Powers of two and
+ * threads <= tile size (tail lanes are not linear). */
+int tg_layout_cooperative(const int shape[2], int threads, const int order[2], tg_layout** out);
+
+/* Register tile (pbelevich.github.io Part 16, "A strided ownership rule":
+ * logical = thread + register * thread_shape) -> (register, thread) ->
+ * (dim0, dim1); thread ids are row-major over thread_shape, register ids
+ * row-major over logical/thread_shape.  Powers of two. */
+int tg_layout_register_tile(const int logical[2], const int thread_shape[2], tg_layout** out);
+
+/* Shared-memory 128-byte XOR swizzle of a tile with 128-byte rows of
+ * elem_bytes-wide elements: (offset) -> (row, col), offset counted in
+ * elements; the 16-byte chunk index of each row is XORed with row mod 8.
+ * rows a power of two >= 8. */
+int tg_layout_swizzle128(int rows, int elem_bytes, tg_layout** out);
+
+/* Accumulator readout of a 128 x bn fp32 tile through tcgen05.ld 32x32b by
+ * four warps: (register, lane, warp) -> (m, n) with m = 32*(warp%4) + lane,
+ * n = register.  bn a power of two in 32..256. */
+int tg_layout_tmem_32x32b(int bn, tg_layout** out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TILEGEMM_H */

@@ -18,3 +18,16 @@ def load_golden(name):
     import json
     with open(os.path.join(GOLDEN, name)) as f:
         return json.load(f)
+
+
+@pytest.fixture(scope="session")
+def tg():
+    """The Python binding, with libtilegemm built in-tree first (nvcc, sm_103a)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_tg_build", os.path.join(ROOT, "tiled_gemm_layouts_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+    import tiled_gemm_layouts_gb300 as tgmod
+    return tgmod

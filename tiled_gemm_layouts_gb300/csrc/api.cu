@@ -1,0 +1,406 @@
+// api.cu -- host side of tg_gemm: argument checks, device and pointer
+// checks, tile selection, tensor-map encoding and the single launch.
+//
+// Checks follow ninetoothed.org "Named layouts", section "Runtime and
+// compilation": logical sizes and input strides positive, non-contiguous
+// inputs allowed, output writes provably non-overlapping, output storage
+// disjoint from every input, all checks before any kernel work, and an
+// unprovable case is an error.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/tilegemm.h"
+#include "gemm_params.h"
+#include "select.h"
+
+namespace tg {
+
+// Device status word: kernels record the first watchdog expiry here.
+__device__ int g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = 2147483647LL;
+constexpr long long kDefaultTimeout = 4000000000LL;
+
+std::atomic<long long> g_timeout{kDefaultTimeout};
+std::atomic<long long> g_skip_kblock{-1};
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int sms = 0;
+    int* status = nullptr;  // device address of g_device_status
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*AddressRangeFn)(CUdeviceptr*, size_t*, CUdeviceptr);
+EncodeTiledFn g_encode = nullptr;
+AddressRangeFn g_range = nullptr;
+std::once_flag g_driver_once;
+
+void load_driver_entry_points() {
+    std::call_once(g_driver_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_range = reinterpret_cast<AddressRangeFn>(fn);
+    });
+}
+
+// Current device, checked for tcgen05 (compute capability 10.x) once.
+int current_device(int* dev_out, DeviceInfo** info_out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return TG_ERR_UNSUPPORTED_DEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return TG_ERR_UNSUPPORTED_DEVICE;
+        }
+        d.supported = (major == 10 && minor == 3);  // the library is built for sm_103a only
+        d.sms = sms;
+        if (d.supported) {
+            void* addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) {
+                cudaGetLastError();
+                return TG_ERR_CUDA;
+            }
+            d.status = static_cast<int*>(addr);
+        }
+        d.ready = true;
+    }
+    if (!d.supported) return TG_ERR_UNSUPPORTED_DEVICE;
+    *dev_out = dev;
+    *info_out = &d;
+    return TG_OK;
+}
+
+typedef unsigned __int128 u128;
+
+struct Span {
+    uintptr_t lo = 0;
+    u128 hi = 0;  // exclusive
+    bool present = false;
+};
+
+// Bytes [p, p + ((rows-1)*ld + width) * 2) of a row-strided 16-bit matrix.
+Span span_of(const void* p, int64_t rows, int64_t width, int64_t ld) {
+    Span s;
+    if (!p) return s;
+    s.present = true;
+    s.lo = reinterpret_cast<uintptr_t>(p);
+    s.hi = (u128)s.lo + ((u128)(rows - 1) * (u128)ld + (u128)width) * 2u;
+    return s;
+}
+
+bool intersects(const Span& a, const Span& b) {
+    if (!a.present || !b.present) return false;
+    return (u128)a.lo < b.hi && (u128)b.lo < a.hi;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Args {
+    int64_t M, N, K;
+    const void* A;
+    int64_t lda;
+    int permA;
+    const void* B;
+    int64_t ldb;
+    int permB;
+    void* C;
+    int64_t ldc;
+    int dtype;
+    const void *bias, *scale, *resid;
+    int64_t ldr;
+    int relu;
+};
+
+// Checks that need no device: sizes, enums, strides, alignment, overlap.
+int check_shape(int64_t M, int64_t N, int64_t K, int dtype, int permA, int permB,
+                const tg_epilogue* epi) {
+    if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return TG_ERR_INVALID_ARG;
+    if ((permA != TG_OP_N && permA != TG_OP_T) || (permB != TG_OP_N && permB != TG_OP_T))
+        return TG_ERR_INVALID_ARG;
+    if (epi && epi->relu != 0 && epi->relu != 1) return TG_ERR_INVALID_ARG;
+    if (dtype != TG_F16 && dtype != TG_BF16) return TG_ERR_DTYPE;
+    return TG_OK;
+}
+
+int check_args(const Args& a) {
+    if (!a.A || !a.B || !a.C) return TG_ERR_INVALID_ARG;
+    const int64_t a_rows = a.permA == TG_OP_N ? a.M : a.K, a_w = a.permA == TG_OP_N ? a.K : a.M;
+    const int64_t b_rows = a.permB == TG_OP_N ? a.K : a.N, b_w = a.permB == TG_OP_N ? a.N : a.K;
+    // Leading dimensions: >= row width (so rows never overlap), and below the
+    // tensor-map stride limit of 2^40 bytes.
+    constexpr int64_t kMaxLd = (1LL << 39) - 8;
+    if (a.lda < a_w || a.ldb < b_w || a.ldc < a.N || a.lda > kMaxLd || a.ldb > kMaxLd ||
+        a.ldc > kMaxLd)
+        return TG_ERR_STRIDE;
+    if (a.resid && (a.ldr < a.N || a.ldr > kMaxLd)) return TG_ERR_STRIDE;
+    if (!aligned16(a.A) || !aligned16(a.B) || !aligned16(a.C) || (a.lda * 2) % 16 ||
+        (a.ldb * 2) % 16 || (a.ldc * 2) % 16)
+        return TG_ERR_ALIGN;
+    if ((a.bias && !aligned16(a.bias)) || (a.scale && !aligned16(a.scale)))
+        return TG_ERR_ALIGN;
+    if (a.resid && (!aligned16(a.resid) || (a.ldr * 2) % 16)) return TG_ERR_ALIGN;
+    const Span c = span_of(a.C, a.M, a.N, a.ldc);
+    const Span ins[5] = {span_of(a.A, a_rows, a_w, a.lda), span_of(a.B, b_rows, b_w, a.ldb),
+                         span_of(a.bias, 1, a.N, a.N), span_of(a.scale, 1, a.M, a.M),
+                         span_of(a.resid, a.M, a.N, a.ldr)};
+    for (const Span& s : ins)
+        if (intersects(c, s)) return TG_ERR_OVERLAP;
+    return TG_OK;
+}
+
+// The touched bytes of every operand must lie inside one allocation of the
+// current device (proves the kernel cannot read or write outside caller memory).
+int check_pointer(const void* p, const Span& s, int dev) {
+    if (!p) return TG_OK;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_POINTER;
+    }
+    if ((at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) || at.device != dev)
+        return TG_ERR_POINTER;
+    if (!g_range) return TG_ERR_POINTER;
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    if (g_range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS)
+        return TG_ERR_POINTER;
+    if ((u128)s.lo < (u128)base || s.hi > (u128)base + size) return TG_ERR_POINTER;
+    return TG_OK;
+}
+
+int check_pointers(const Args& a, int dev) {
+    const int64_t a_rows = a.permA == TG_OP_N ? a.M : a.K, a_w = a.permA == TG_OP_N ? a.K : a.M;
+    const int64_t b_rows = a.permB == TG_OP_N ? a.K : a.N, b_w = a.permB == TG_OP_N ? a.N : a.K;
+    int rc;
+    if ((rc = check_pointer(a.A, span_of(a.A, a_rows, a_w, a.lda), dev))) return rc;
+    if ((rc = check_pointer(a.B, span_of(a.B, b_rows, b_w, a.ldb), dev))) return rc;
+    if ((rc = check_pointer(a.C, span_of(a.C, a.M, a.N, a.ldc), dev))) return rc;
+    if ((rc = check_pointer(a.bias, span_of(a.bias, 1, a.N, a.N), dev))) return rc;
+    if ((rc = check_pointer(a.scale, span_of(a.scale, 1, a.M, a.M), dev))) return rc;
+    if ((rc = check_pointer(a.resid, span_of(a.resid, a.M, a.N, a.ldr), dev))) return rc;
+    return TG_OK;
+}
+
+bool encode_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner, uint64_t outer,
+               int64_t ld, uint32_t box_inner, uint32_t box_outer) {
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt =
+        dtype == TG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand tensor map.  `rows` x `k` operand; if mn_major the storage has the
+// rows dimension contiguous (dims {rows, K}), else K contiguous (dims {K, rows}).
+bool encode_operand(CUtensorMap* map, int dtype, const void* base, int64_t rows, int64_t k,
+                    int64_t ld, bool mn_major, int box_rows) {
+    if (mn_major) return encode_2d(map, dtype, base, rows, k, ld, 64, 64);
+    return encode_2d(map, dtype, base, k, rows, ld, 64, box_rows);
+}
+
+uint32_t make_idesc(int dtype, bool p_mn, bool q_mn, int n, int m) {
+    const uint32_t fmt = dtype == TG_BF16 ? 1u : 0u;
+    return (1u << 4)                   // accumulator format: fp32
+           | (fmt << 7) | (fmt << 10)  // A and B: fp16 or bf16 (always the same type)
+           | ((p_mn ? 1u : 0u) << 15) | ((q_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+}  // namespace
+
+int gemm_impl(const Args& a, cudaStream_t stream) {
+    int rc = check_shape(a.M, a.N, a.K, a.dtype, a.permA, a.permB, nullptr);
+    if (rc) return rc;
+    if (a.relu != 0 && a.relu != 1) return TG_ERR_INVALID_ARG;
+    if ((rc = check_args(a))) return rc;
+    int dev;
+    DeviceInfo* info;
+    if ((rc = current_device(&dev, &info))) return rc;
+    load_driver_entry_points();
+    if (!g_encode) return TG_ERR_CUDA;
+    if ((rc = check_pointers(a, dev))) return rc;
+
+    const KernelConfig cfg = select_config(a.M, a.N, a.K, a.dtype, a.permA, a.permB,
+                                           a.bias != nullptr || a.scale != nullptr ||
+                                               a.resid != nullptr || a.relu,
+                                           info->sms);
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    const bool swap = cfg.swap != 0;
+    p.Mk = (int)(swap ? a.N : a.M);
+    p.Nk = (int)(swap ? a.M : a.N);
+    p.K = (int)a.K;
+    p.num_kb = (int)((a.K + 63) / 64);
+    p.tiles_m = (p.Mk + cfg.bm - 1) / cfg.bm;
+    p.tiles_n = (p.Nk + cfg.bn - 1) / cfg.bn;
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.group_m = cfg.group_m;
+    // Which operand storage has the kernel's row (P) / column (Q) index contiguous.
+    bool p_mn, q_mn;
+    bool ok;
+    if (!swap) {
+        p_mn = a.permA == TG_OP_T;  // A stored K x M
+        q_mn = a.permB == TG_OP_N;  // B stored K x N
+        ok = encode_operand(&p.map_p, a.dtype, a.A, a.M, a.K, a.lda, p_mn, 128) &&
+             encode_operand(&p.map_q, a.dtype, a.B, a.N, a.K, a.ldb, q_mn, cfg.bn);
+    } else {
+        p_mn = a.permB == TG_OP_N;  // P = B^T: rows n contiguous when B is K x N
+        q_mn = a.permA == TG_OP_T;  // Q = A^T: columns m contiguous when A is K x M
+        ok = encode_operand(&p.map_p, a.dtype, a.B, a.N, a.K, a.ldb, p_mn, 128) &&
+             encode_operand(&p.map_q, a.dtype, a.A, a.M, a.K, a.lda, q_mn, cfg.bn);
+    }
+    if (!ok) return TG_ERR_CUDA;
+    p.p_mn_major = p_mn;
+    p.q_mn_major = q_mn;
+    p.idesc = make_idesc(a.dtype, p_mn, q_mn, cfg.bn, 128);
+    p.swap = swap;
+    p.bf16 = a.dtype == TG_BF16;
+    p.M = (int)a.M;
+    p.N = (int)a.N;
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.bias_n = a.bias;
+    p.scale_m = a.scale;
+    p.resid = a.resid;
+    p.ldr = a.ldr;
+    p.relu = a.relu;
+    p.timeout_cycles = g_timeout.load();
+    p.status = info->status;
+    p.inject_skip_load = (int)g_skip_kblock.load();
+    const cudaError_t e = launch_gemm(p, cfg, info->sms, stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_CUDA;
+    }
+    return TG_OK;
+}
+
+}  // namespace tg
+
+using namespace tg;
+
+extern "C" int tg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                       tg_perm permA, const void* B, int64_t ldb, tg_perm permB, void* C,
+                       int64_t ldc, tg_dtype dtype, const tg_epilogue* epi,
+                       cudaStream_t stream) {
+    Args a;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.A = A;
+    a.lda = lda;
+    a.permA = (int)permA;
+    a.B = B;
+    a.ldb = ldb;
+    a.permB = (int)permB;
+    a.C = C;
+    a.ldc = ldc;
+    a.dtype = (int)dtype;
+    a.bias = epi ? epi->bias_n : nullptr;
+    a.scale = epi ? epi->scale_m : nullptr;
+    a.resid = epi ? epi->residual : nullptr;
+    a.ldr = (epi && epi->residual) ? (epi->ldr ? epi->ldr : ldc) : 0;
+    a.relu = epi ? epi->relu : 0;
+    return gemm_impl(a, stream);
+}
+
+extern "C" const char* tg_status_string(int status) {
+    switch (status) {
+        case TG_OK: return "TG_OK";
+        case TG_ERR_INVALID_ARG: return "TG_ERR_INVALID_ARG";
+        case TG_ERR_STRIDE: return "TG_ERR_STRIDE";
+        case TG_ERR_ALIGN: return "TG_ERR_ALIGN";
+        case TG_ERR_OVERLAP: return "TG_ERR_OVERLAP";
+        case TG_ERR_DTYPE: return "TG_ERR_DTYPE";
+        case TG_ERR_UNSUPPORTED_DEVICE: return "TG_ERR_UNSUPPORTED_DEVICE";
+        case TG_ERR_CUDA: return "TG_ERR_CUDA";
+        case TG_ERR_TIMEOUT: return "TG_ERR_TIMEOUT";
+        case TG_ERR_POINTER: return "TG_ERR_POINTER";
+        case TG_ERR_LAYOUT: return "TG_ERR_LAYOUT";
+        case TG_ERR_BUFFER: return "TG_ERR_BUFFER";
+        default: return "TG_ERR_UNKNOWN";
+    }
+}
+
+extern "C" int tg_query_config(int64_t M, int64_t N, int64_t K, tg_dtype dtype, tg_perm permA,
+                               tg_perm permB, const tg_epilogue* epi, char* buf, size_t len) {
+    int rc = check_shape(M, N, K, (int)dtype, (int)permA, (int)permB, epi);
+    if (rc) return rc;
+    if (!buf) return TG_ERR_INVALID_ARG;
+    int dev;
+    DeviceInfo* info;
+    if ((rc = current_device(&dev, &info))) return rc;
+    const bool has_epi = epi && (epi->bias_n || epi->scale_m || epi->residual || epi->relu);
+    const KernelConfig c = select_config(M, N, K, (int)dtype, (int)permA, (int)permB, has_epi,
+                                         info->sms);
+    const std::string s = describe_config(c);
+    if (s.size() + 1 > len) return TG_ERR_BUFFER;
+    std::memcpy(buf, s.c_str(), s.size() + 1);
+    return TG_OK;
+}
+
+extern "C" int tg_debug_status(int* detail) {
+    int dev;
+    DeviceInfo* info;
+    int rc = current_device(&dev, &info);
+    if (rc) return rc;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_CUDA;
+    }
+    int v = 0;
+    const int zero = 0;
+    if (cudaMemcpy(&v, info->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(info->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_CUDA;
+    }
+    if (detail) *detail = v;
+    return v == 0 ? TG_OK : TG_ERR_TIMEOUT;
+}
+
+extern "C" int tg_debug_configure(int64_t timeout_cycles, int64_t skip_kblock) {
+    if (timeout_cycles < 0 || skip_kblock < -1) return TG_ERR_INVALID_ARG;
+    g_timeout.store(timeout_cycles == 0 ? kDefaultTimeout : (long long)timeout_cycles);
+    g_skip_kblock.store((long long)skip_kblock);
+    return TG_OK;
+}

@@ -1,0 +1,69 @@
+// gemm_params.h -- what the host side hands to the tcgen05 GEMM kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace tg {
+
+// Device status word values (the kernel records the first failure it sees).
+enum : int {
+    DEV_OK = 0,
+    DEV_TIMEOUT_PRODUCER = 0x100,   // + which wait
+    DEV_TIMEOUT_MMA = 0x200,
+    DEV_TIMEOUT_EPILOGUE = 0x300,
+};
+
+// The kernel computes D = P * Q over a (Mk x Nk) output in tiles of
+// BM x BN, contracting over K in blocks of 64.  Without operand swap P = A,
+// Q = B and D = C; with swap P = B^T, Q = A^T and D = C^T (the output is then
+// written transposed, so C is still M x N row-major).
+struct alignas(128) GemmParams {
+    CUtensorMap map_p;   // P operand: K-major box {64, BM} or MN-major box {64, 64}
+    CUtensorMap map_q;   // Q operand: K-major box {64, BN} or MN-major box {64, 64}
+    int Mk, Nk, K;       // kernel-side problem (after the optional swap)
+    int num_kb;          // ceil(K / 64)
+    int tiles_m, tiles_n, num_tiles;
+    int group_m;         // raster: tile rows per group
+    uint32_t idesc;      // tcgen05 instruction descriptor (dtype, majors, N, M)
+    int p_mn_major;      // 1: P tile stored MN-major in shared memory
+    int q_mn_major;
+    int swap;            // 1: D is C^T
+    int bf16;            // element type of every operand: 0 fp16, 1 bf16
+    // epilogue, in C's (m, n) coordinates
+    int M, N;            // C is M x N
+    void* C;
+    long long ldc;
+    const void* bias_n;  // [N] or null
+    const void* scale_m; // [M] or null
+    const void* resid;   // [M, ldr] or null
+    long long ldr;
+    int relu;
+    // watchdog
+    long long timeout_cycles;
+    int* status;         // device status word
+    int inject_skip_load;// test hook: producer never arms this k-block (-1 = off)
+};
+
+// Tile / pipeline configuration chosen by the selector.
+struct KernelConfig {
+    int swap;       // compute C^T = B^T A^T
+    int bm;         // 128 (one CTA) or 256 (CTA pair)
+    int bn;         // 32, 64, 128 or 256
+    int pair;       // 1: cta_group::2 on a 2-CTA cluster
+    int stages;
+    int group_m;
+    int grid;       // persistent CTAs
+    int tiles;
+};
+
+// Launches one persistent GEMM; returns a cudaError_t.
+cudaError_t launch_gemm(const GemmParams& p, const KernelConfig& cfg, int num_sms,
+                        cudaStream_t stream);
+
+// Dynamic shared memory (bytes) and ring depth of a configuration.
+int gemm_smem_bytes(int bn, int stages, int pair);
+int gemm_stages(int bn);
+
+}  // namespace tg
