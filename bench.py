@@ -157,6 +157,7 @@ def workload_specs():
     return {
         "fp16_4096": dict(M=4096, N=4096, K=4096, dtype=S.F16, seed=1002),
         "bf16_4096": dict(M=4096, N=4096, K=4096, dtype=S.BF16, seed=1002),
+        "fp16_4096x4096x8192": dict(M=4096, N=4096, K=8192, dtype=S.F16, seed=1002),
         "fp16_8192x8192x4096_fused": dict(M=8192, N=8192, K=4096, dtype=S.F16, seed=1003,
                                           bias=True, scale=True, residual=True, relu=True),
         "fp16_8192x8192x4096_plain": dict(M=8192, N=8192, K=4096, dtype=S.F16, seed=1003),

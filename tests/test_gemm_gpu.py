@@ -58,11 +58,12 @@ def test_edges(tg, M, N, K, dtype):
 @pytest.mark.parametrize("dtype", [F16, BF16])
 def test_permutes_and_strides(tg, permA, permB, dtype):
     M, N, K = 300, 260, 400
-    lda = (K if permA == 0 else M) + 24
-    ldb = (N if permB == 0 else K) + 64
+    up8 = lambda x: -(-x // 8) * 8  # row strides must be whole 16-byte units
+    lda = up8(K if permA == 0 else M) + 24
+    ldb = up8(N if permB == 0 else K) + 64
     p = synthetic.gemm_problem(M, N, K, dtype, 11 + 2 * permA + permB, permA=permA, permB=permB,
                                lda=lda, ldb=ldb, dist="normal", sigma=0.5)
-    full_check(tg, p, ldc=N + 8, what=f"perm {permA}{permB}")
+    full_check(tg, p, ldc=up8(N) + 8, what=f"perm {permA}{permB}")
 
 
 EPILOGUES = [
@@ -81,7 +82,7 @@ def test_epilogue_combinations(tg, epi, dtype):
     p = synthetic.gemm_problem(M, N, K, dtype, 21, ldr=N + 8 if flags.get("residual") else None,
                                **flags)
     p["relu"] = relu
-    full_check(tg, p, ldc=N + 24, what=str(epi))
+    full_check(tg, p, ldc=N + 24, what=str(epi))  # N = 200: both strides whole 16-byte units
 
 
 @pytest.mark.parametrize("force", ["bn=32,swap=1", "bn=64,swap=1", "bn=128,swap=1",
@@ -89,7 +90,7 @@ def test_epilogue_combinations(tg, epi, dtype):
                                    "bn=256,swap=0", "bn=128,group_m=1", "bn=256,grid=7"])
 @pytest.mark.parametrize("permA,permB", [(0, 0), (1, 1)])
 def test_every_tile_configuration(tg, force, permA, permB):
-    M, N, K = 190, 330, 260
+    M, N, K = 184, 328, 264  # ragged against every tile; dense strides stay 16-byte units
     p = synthetic.gemm_problem(M, N, K, BF16, 31, permA=permA, permB=permB,
                                bias=True, scale=True, residual=True)
     p["relu"] = True
