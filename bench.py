@@ -65,9 +65,10 @@ def profiled_traffic(workload_key: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    """nvidia-smi clock / throttle samples every 20 ms; summary() keeps the
+    samples whose timestamps fall inside the marked window."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -75,12 +76,13 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.window = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -88,12 +90,19 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def started(self, timeout=3.0) -> bool:
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.01)
+        return bool(self.lines)
+
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.1)  # let the samples of the window's last moments arrive
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -102,24 +111,33 @@ class ClockSampler:
             self.t.join(timeout=2)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        import datetime
+        rows = []
         for line in self.lines:
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
+        if self.window is not None:
+            lo, hi = self.window
+            inside = [r for r in rows if lo - 0.03 <= r[0] <= hi + 0.03]
+        else:
+            inside = rows
+        if not inside:
+            return None
+        reasons = set()
+        for r in inside:
             for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
-                                "sw_power_cap"), parts[5:9]):
+                                "sw_power_cap"), r[3]):
                 if v.lower().startswith("active"):
                     reasons.add(name)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": sorted(reasons),
+                "samples": len(inside)}
 
 
 # --------------------------------------------------------------------------
@@ -279,8 +297,8 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the other workloads and the CPU baseline (for profiling)")
@@ -317,10 +335,13 @@ def main():
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.started()
         t_wall0 = time.perf_counter()
+        w0 = time.time()
         times = time_kernel(prob.call, args.steps, args.warmup, flush, stream)
         torch.cuda.synchronize()
         barrier(world)
+        clk.window = (w0, time.time())
         wall = time.perf_counter() - t_wall0
     st, code = tg.tg_debug_status()
     if st != tg.TG_OK:

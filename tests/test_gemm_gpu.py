@@ -85,9 +85,31 @@ def test_epilogue_combinations(tg, epi, dtype):
     full_check(tg, p, ldc=N + 24, what=str(epi))  # N = 200: both strides whole 16-byte units
 
 
-@pytest.mark.parametrize("force", ["bn=32,swap=1", "bn=64,swap=1", "bn=128,swap=1",
-                                   "bn=256,swap=1", "bn=64,swap=0", "bn=128,swap=0",
-                                   "bn=256,swap=0", "bn=128,group_m=1", "bn=256,grid=7"])
+CONFIGS = [
+    "pair=0,bn=32,swap=1", "pair=0,bn=64,swap=1", "pair=0,bn=128,swap=1", "pair=0,bn=256,swap=1",
+    "pair=0,bn=64,swap=0", "pair=0,bn=128,swap=0", "pair=0,bn=192,swap=0", "pair=0,bn=224,swap=0",
+    "pair=0,bn=256,swap=0", "pair=0,bn=128,group_m=1", "pair=0,bn=256,grid=7",
+    "pair=1,bn=128,swap=0", "pair=1,bn=192,swap=0", "pair=1,bn=224,swap=0", "pair=1,bn=256,swap=0",
+    "pair=1,bn=224,swap=1", "pair=1,bn=256,swap=1", "pair=1,bn=256,grid=6", "pair=1,bn=128,group_m=1",
+]
+
+
+def test_selector_reports_forced_configuration(tg):
+    import os
+    old = os.environ.get("TG_FORCE_CONFIG")
+    try:
+        os.environ["TG_FORCE_CONFIG"] = "pair=1,bn=224,swap=0"
+        cfg = tg.parse_config(tg.tg_query_config(4096, 4096, 4096, F16))
+        assert (cfg["pair"], cfg["bn"], cfg["bm"], cfg["swap"]) == (1, 224, 256, 0)
+        assert cfg["grid"] % 2 == 0
+    finally:
+        if old is None:
+            os.environ.pop("TG_FORCE_CONFIG", None)
+        else:
+            os.environ["TG_FORCE_CONFIG"] = old
+
+
+@pytest.mark.parametrize("force", CONFIGS)
 @pytest.mark.parametrize("permA,permB", [(0, 0), (1, 1)])
 def test_every_tile_configuration(tg, force, permA, permB):
     M, N, K = 184, 328, 264  # ragged against every tile; dense strides stay 16-byte units
@@ -152,14 +174,15 @@ def test_pointer_checks_on_device(tg):
     assert tg.tg_gemm(64, 64, 64, A, 64, 0, A, 64, 0, A, 64, F16) == tg.TG_ERR_OVERLAP
 
 
-def test_watchdog_expires_and_context_survives(tg):
+@pytest.mark.parametrize("force", ["pair=0,bn=128", "pair=1,bn=256"])
+def test_watchdog_expires_and_context_survives(tg, force):
     """A producer that never arms one k-block makes the MMA wait run out: the
     kernel must return with TG_ERR_TIMEOUT instead of hanging, and the next
     call must work normally."""
     p = synthetic.gemm_problem(256, 256, 1024, F16, 81)
     assert tg.tg_debug_configure(1_000_000, 3) == tg.TG_OK
     try:
-        _, rc = run_gemm(tg, p)
+        _, rc = run_gemm(tg, p, force=force)
         assert rc == tg.TG_OK
         st, code = tg.tg_debug_status()
         assert st == tg.TG_ERR_TIMEOUT and code != 0

@@ -277,21 +277,24 @@ int gemm_impl(const Args& a, cudaStream_t stream) {
     // Which operand storage has the kernel's row (P) / column (Q) index contiguous.
     bool p_mn, q_mn;
     bool ok;
+    // Each CTA stages 128 rows of P and q_box columns of Q (half the tile's
+    // columns when a CTA pair shares the tile).
+    const int q_box = cfg.pair ? cfg.bn / 2 : cfg.bn;
     if (!swap) {
         p_mn = a.permA == TG_OP_T;  // A stored K x M
         q_mn = a.permB == TG_OP_N;  // B stored K x N
         ok = encode_operand(&p.map_p, a.dtype, a.A, a.M, a.K, a.lda, p_mn, 128) &&
-             encode_operand(&p.map_q, a.dtype, a.B, a.N, a.K, a.ldb, q_mn, cfg.bn);
+             encode_operand(&p.map_q, a.dtype, a.B, a.N, a.K, a.ldb, q_mn, q_box);
     } else {
         p_mn = a.permB == TG_OP_N;  // P = B^T: rows n contiguous when B is K x N
         q_mn = a.permA == TG_OP_T;  // Q = A^T: columns m contiguous when A is K x M
         ok = encode_operand(&p.map_p, a.dtype, a.B, a.N, a.K, a.ldb, p_mn, 128) &&
-             encode_operand(&p.map_q, a.dtype, a.A, a.M, a.K, a.lda, q_mn, cfg.bn);
+             encode_operand(&p.map_q, a.dtype, a.A, a.M, a.K, a.lda, q_mn, q_box);
     }
     if (!ok) return TG_ERR_CUDA;
     p.p_mn_major = p_mn;
     p.q_mn_major = q_mn;
-    p.idesc = make_idesc(a.dtype, p_mn, q_mn, cfg.bn, 128);
+    p.idesc = make_idesc(a.dtype, p_mn, q_mn, cfg.bn, cfg.bm);
     p.swap = swap;
     p.bf16 = a.dtype == TG_BF16;
     p.M = (int)a.M;

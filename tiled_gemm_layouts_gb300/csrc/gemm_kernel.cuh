@@ -10,16 +10,24 @@
 //   warp 0      TMA producer: fills an S-stage ring of 128B-swizzled shared
 //               tiles, one mbarrier "full"/"empty" pair per stage.  Tails of
 //               M, N and K are zero-filled by the tensor map, so they add 0.
-//   warp 1      owns TMEM; one thread issues tcgen05.mma (M=128, N=BN, K=16)
-//               into a double-buffered fp32 accumulator in tensor memory.
+//   warp 1      owns TMEM; one thread issues tcgen05.mma (K=16 per
+//               instruction) into a double-buffered fp32 accumulator.
 //   warps 2..5  epilogue: tcgen05.ld 32x32b (thread t of warp w holds TMEM
 //               lane 32*(w%4)+t = tile row, register j = tile column), applies
 //               the epilogue in fp32 and stores with per-element edge masks,
 //               while the next tile's main loop already runs in the other
 //               accumulator buffer.
+// PAIR = true runs each 256 x BN tile on a cluster of two CTAs with
+// tcgen05.mma.cta_group::2: CTA r holds rows 128r..128r+127 of the A block and
+// columns r*BN/2 .. (r+1)*BN/2-1 of the B block, so each SM stages half the
+// operand bytes of a single-CTA 128 x BN tile per flop.  The leader (rank 0)
+// issues the MMAs; both producers signal the leader's "full" barrier, the
+// MMA completion is multicast to both CTAs' "empty"/"tmem full" barriers, and
+// both epilogues release the accumulator on the leader's "tmem empty".
 // Every wait is bounded: after p.timeout_cycles the waiting thread records a
-// status code, raises a CTA-wide abort flag, every role drains what it has in
-// flight (TMA loads, MMAs), TMEM is freed and the kernel returns.
+// status code, raises the abort flag of its CTA (and of the peer), every role
+// drains what it has in flight (TMA loads, MMAs), TMEM is freed and the
+// kernel returns.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -30,27 +38,42 @@
 
 namespace tg {
 
-constexpr int kBM = 128;       // accumulator rows per CTA (TMEM lanes)
 constexpr int kBK = 64;        // K elements per stage: one 128-byte swizzle row of fp16/bf16
 constexpr int kUmmaK = 16;     // K per tcgen05.mma of kind::f16
 constexpr int kThreads = 192;  // producer warp, MMA warp, four epilogue warps
 
-template <int BN>
+template <int BN, bool PAIR>
 struct TileShape {
-    static constexpr int kAStage = kBM * kBK * 2;  // 16 KB
-    static constexpr int kBStage = BN * kBK * 2;
+    static constexpr int kBM = PAIR ? 256 : 128;              // rows per tile (whole cluster)
+    static constexpr int kBNC = PAIR ? BN / 2 : BN;           // B columns staged per CTA
+    static constexpr int kBBoxes = (kBNC + 63) / 64;          // 64-column swizzle atoms
+    static constexpr int kAStage = 128 * kBK * 2;             // 16 KB
+    static constexpr int kBStage = kBBoxes * 64 * kBK * 2;    // whole atoms
     static constexpr int kStage = kAStage + kBStage;
-    static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;  // two accumulator buffers
+    static constexpr int kStages = (200 * 1024 / kStage) > 8 ? 8 : (200 * 1024 / kStage);
+    static constexpr int kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
+                                   : 2 * BN <= 256 ? 256 : 512;
+    static constexpr int kSmemBytes = 1024 + kStages * kStage + (2 * kStages + 5) * 8 + 16;
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN: multiple of 32 in 32..256");
+    static_assert(!PAIR || BN % 32 == 0, "pair tiles split BN in halves of 16-multiples");
 };
 
 struct Watch {
     volatile int* abort;
+    uint32_t peer_abort;  // shared::cluster address of the peer's flag (PAIR only)
+    bool pair;
     int* status;
     long long timeout;
 };
 
+__device__ __forceinline__ void raise_abort(const Watch& w, int code) {
+    *w.abort = 1;
+    if (w.pair) st_shared_cluster_u32(w.peer_abort, 1);
+    atomicCAS(w.status, 0, code);
+}
+
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or
-// this wait ran out of time (then it raises the abort flag and records `code`).
+// this wait ran out of time (then it raises the abort flags and records `code`).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Watch& w, int code) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
@@ -58,8 +81,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
         if (mbar_try_wait(bar, parity)) return true;
         if (*w.abort) return false;
         if (clock64() - t0 > w.timeout) {
-            *w.abort = 1;
-            atomicCAS(w.status, 0, code);
+            raise_abort(w, code);
             return false;
         }
     }
@@ -105,7 +127,7 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8], int bf16)
 }
 
 // Epilogue for one 32-column chunk held by this thread: kernel row `rk`
-// (one TMEM lane), kernel columns c0 .. c0+31 in acc[].
+// (one TMEM lane), kernel columns c0 .. c0+31 in y[].
 __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int rk, int c0,
                                                float (&y)[32], float row_scale, float row_bias) {
     const int bf = p.bf16;
@@ -190,11 +212,13 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int rk, int 
     }
 }
 
-template <int BN, int STAGES>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
-    using TS = TileShape<BN>;
+    using TS = TileShape<BN, PAIR>;
+    constexpr int STAGES = TS::kStages;
+    constexpr int CG = PAIR ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
-    // 1024-byte alignment for the 128B-swizzle atoms
+    // 1024-byte alignment for the 128B-swizzle atoms (same offset in both CTAs of a pair)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint8_t* sA = smem;
@@ -210,7 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const Watch w{abort_flag, p.status, p.timeout_cycles};
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+    const bool leader = rank == 0;
+    const int cta_tile0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // first tile
+    const int tile_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const Watch w{abort_flag,
+                  PAIR ? mapa_shared(smem_addr((const void*)abort_flag), rank ^ 1u) : 0u, PAIR,
+                  p.status, p.timeout_cycles};
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&p.map_p);
@@ -221,18 +251,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&tfull[b]), 1);
-            mbar_init(smem_addr(&tempty[b]), 4 * 32);
+            mbar_init(smem_addr(&tempty[b]), PAIR ? 8 : 4);  // one arrival per epilogue warp
         }
         mbar_init(smem_addr(drain), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc<1>(smem_addr(tmem_slot), TS::kTmemCols);
-        tmem_relinquish<1>();
+        tmem_alloc<CG>(smem_addr(tmem_slot), TS::kTmemCols);
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync();  // the peer's barriers exist before anyone signals them
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -244,36 +277,58 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             uint32_t armed = 0, armed_parity = 0;
             long long g = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            // bytes this CTA lands per stage (A half + its B columns)
+            const uint32_t a_bytes = TS::kAStage;
+            const uint32_t b_bytes = p.q_mn_major ? (uint32_t)TS::kBStage : (uint32_t)TS::kBNC * 128u;
+            const uint32_t stage_tx = (a_bytes + b_bytes) * (PAIR ? 2u : 1u);
+            for (int t = cta_tile0; ok && t < p.num_tiles; t += tile_step) {
                 int tm, tn;
                 tile_coords(p, t, tm, tn);
-                const int m0 = tm * kBM, n0 = tn * BN;
+                const int m0 = tm * TS::kBM + (int)rank * 128;
+                const int n0 = tn * BN + (int)rank * TS::kBNC;
                 for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
                     if (!wait_bar(smem_addr(&empty[stage]), phase ^ 1, w, DEV_TIMEOUT_PRODUCER)) {
                         ok = false;
                         break;
                     }
                     if (g != p.inject_skip_load) {
-                        const uint32_t fb = smem_addr(&full[stage]);
-                        mbar_arrive_expect_tx(fb, TS::kStage);
-                        armed |= 1u << stage;
-                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                        const uint32_t fb_local = smem_addr(&full[stage]);
+                        if (leader) {
+                            mbar_arrive_expect_tx(fb_local, stage_tx);
+                            armed |= 1u << stage;
+                            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                        }
+                        const uint32_t fb = PAIR ? mapa_shared(fb_local, 0) : fb_local;
                         const uint32_t a_dst = smem_addr(sA + stage * TS::kAStage);
                         const uint32_t b_dst = smem_addr(sB + stage * TS::kBStage);
                         const int k0 = kb * kBK;
                         if (p.p_mn_major) {
 #pragma unroll
-                            for (int j = 0; j < kBM / 64; ++j)
-                                tma_load_2d(a_dst + j * 8192, &p.map_p, fb, m0 + 64 * j, k0);
+                            for (int j = 0; j < 2; ++j) {
+                                if constexpr (PAIR)
+                                    tma_load_2d_pair(a_dst + j * 8192, &p.map_p, fb, m0 + 64 * j, k0);
+                                else
+                                    tma_load_2d(a_dst + j * 8192, &p.map_p, fb, m0 + 64 * j, k0);
+                            }
                         } else {
-                            tma_load_2d(a_dst, &p.map_p, fb, k0, m0);
+                            if constexpr (PAIR)
+                                tma_load_2d_pair(a_dst, &p.map_p, fb, k0, m0);
+                            else
+                                tma_load_2d(a_dst, &p.map_p, fb, k0, m0);
                         }
                         if (p.q_mn_major) {
 #pragma unroll
-                            for (int j = 0; j < BN / 64; ++j)
-                                tma_load_2d(b_dst + j * 8192, &p.map_q, fb, n0 + 64 * j, k0);
+                            for (int j = 0; j < TS::kBBoxes; ++j) {
+                                if constexpr (PAIR)
+                                    tma_load_2d_pair(b_dst + j * 8192, &p.map_q, fb, n0 + 64 * j, k0);
+                                else
+                                    tma_load_2d(b_dst + j * 8192, &p.map_q, fb, n0 + 64 * j, k0);
+                            }
                         } else {
-                            tma_load_2d(b_dst, &p.map_q, fb, k0, n0);
+                            if constexpr (PAIR)
+                                tma_load_2d_pair(b_dst, &p.map_q, fb, k0, n0);
+                            else
+                                tma_load_2d(b_dst, &p.map_q, fb, k0, n0);
                         }
                     }
                     if (++stage == STAGES) {
@@ -284,19 +339,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
             if (*abort_flag) {
                 // No TMA write may land after the CTA exits: wait for the last
-                // armed phase of every stage.
+                // armed phase of every stage (the leader's barriers count the
+                // bytes of both CTAs).
                 for (int s = 0; s < STAGES; ++s)
                     if (armed & (1u << s)) drain_bar(smem_addr(&full[s]), (armed_parity >> s) & 1, w);
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             int i = 0;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++i) {
+            for (int t = cta_tile0; ok && t < p.num_tiles; t += tile_step, ++i) {
                 const int buf = i & 1;
                 const uint32_t aph = (i >> 1) & 1;
                 if (!wait_bar(smem_addr(&tempty[buf]), aph ^ 1, w, DEV_TIMEOUT_MMA + 1)) break;
@@ -320,26 +376,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         const uint64_t bd = p.q_mn_major
                                                 ? smem_desc_sw128(b_addr + kk * 2048, 8192, 1024)
                                                 : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-                        mma_f16<1>(d_tmem, ad, bd, p.idesc, (kb | kk) != 0);
+                        mma_f16<CG>(d_tmem, ad, bd, p.idesc, (kb | kk) != 0);
                     }
-                    mma_commit(smem_addr(&empty[stage]));  // frees the stage once read
+                    // frees the stage (in both CTAs) once the MMAs have read it
+                    if constexpr (PAIR)
+                        mma_commit_pair(smem_addr(&empty[stage]), 0x3);
+                    else
+                        mma_commit(smem_addr(&empty[stage]));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                mma_commit(smem_addr(&tfull[buf]));  // accumulator complete
+                // accumulator complete (in both CTAs' TMEM)
+                if constexpr (PAIR)
+                    mma_commit_pair(smem_addr(&tfull[buf]), 0x3);
+                else
+                    mma_commit(smem_addr(&tfull[buf]));
             }
             // Nothing may still write TMEM when it is released.
-            mma_commit(smem_addr(drain));
+            if constexpr (PAIR)
+                mma_commit_pair_local(smem_addr(drain));
+            else
+                mma_commit(smem_addr(drain));
             drain_bar(smem_addr(drain), 0, w);
         }
     } else {
         // ---------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         int i = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++i) {
+        for (int t = cta_tile0; t < p.num_tiles; t += tile_step, ++i) {
             const int buf = i & 1;
             const uint32_t aph = (i >> 1) & 1;
             int ok = 1;
@@ -349,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tc_fence_after();
             int tm, tn;
             tile_coords(p, t, tm, tn);
-            const int rk = tm * kBM + q * 32 + lane;
+            const int rk = tm * TS::kBM + (int)rank * 128 + q * 32 + lane;
             float row_scale = 1.0f, row_bias = 0.0f;
             if (!p.swap) {
                 if (p.scale_m && rk < p.M) row_scale = to_f32(static_cast<const uint16_t*>(p.scale_m)[rk], p.bf16);
@@ -366,7 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 if (c == BN / 32 - 1) {
                     // every column of this buffer is in registers: release it
                     tc_fence_before();
-                    mbar_arrive(smem_addr(&tempty[buf]));
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (PAIR)
+                            mbar_arrive_cluster(smem_addr(&tempty[buf]), 0);  // leader's barrier
+                        else
+                            mbar_arrive(smem_addr(&tempty[buf]));
+                    }
                 }
                 float y[32];
 #pragma unroll
@@ -377,10 +450,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
 
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    if constexpr (PAIR) {
+        if (*abort_flag) {
+            // the peer's loads for phases the leader never armed cannot be
+            // observed here: give any such copy ample time to land
+            const long long t0 = clock64();
+            while (clock64() - t0 < 2000000) {
+            }
+        }
+        cluster_sync();  // no CTA leaves while its peer may still signal it
+    } else {
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc<1>(tmem_base, TS::kTmemCols);
+        tmem_dealloc<CG>(tmem_base, TS::kTmemCols);
     }
 }
 

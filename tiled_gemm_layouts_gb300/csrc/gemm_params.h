@@ -50,7 +50,7 @@ struct alignas(128) GemmParams {
 struct KernelConfig {
     int swap;       // compute C^T = B^T A^T
     int bm;         // 128 (one CTA) or 256 (CTA pair)
-    int bn;         // 32, 64, 128 or 256
+    int bn;         // tile columns: 32..256, a compiled value (see gemm_launch.cuh)
     int pair;       // 1: cta_group::2 on a 2-CTA cluster
     int stages;
     int group_m;
@@ -62,8 +62,9 @@ struct KernelConfig {
 cudaError_t launch_gemm(const GemmParams& p, const KernelConfig& cfg, int num_sms,
                         cudaStream_t stream);
 
-// Dynamic shared memory (bytes) and ring depth of a configuration.
-int gemm_smem_bytes(int bn, int stages, int pair);
-int gemm_stages(int bn);
+// Dynamic shared memory (bytes) and ring depth of a configuration; -1 if the
+// (bn, pair) combination is not compiled.
+int gemm_smem_bytes(int bn, int pair);
+int gemm_stages(int bn, int pair);
 
 }  // namespace tg

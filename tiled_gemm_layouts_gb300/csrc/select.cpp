@@ -17,32 +17,59 @@ namespace {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Relative MMA-pipe efficiency of a 128 x bn tile: narrower tiles re-read the
-// 128-row operand from shared memory more often per flop.
-double tile_efficiency(int bn) {
+// Relative tensor-pipe efficiency of a tile shape in steady state.  A
+// single-CTA 128 x BN tile stages 16 KB of A and BN*128 bytes of B per 64-deep
+// K block, and the tensor core reads the same bytes back: narrower tiles move
+// more shared-memory bytes per flop and stall on shared-memory bandwidth.  A
+// CTA pair (256 x BN on two SMs) halves the B bytes each SM stages.  Values
+// are calibrated on GB300 measurements of this kernel (4096^3 and
+// 8192 x 8192 x 4096 sweeps over every compiled tile).
+double tile_efficiency(int bn, int pair) {
+    if (pair) {
+        switch (bn) {
+            case 256: return 0.90;
+            case 224: return 0.88;
+            case 192: return 0.84;
+            case 128: return 0.72;
+            default: return 0.5;
+        }
+    }
     switch (bn) {
-        case 256: return 1.0;
-        case 128: return 0.92;
-        case 64: return 0.75;
-        default: return 0.55;
+        case 256: return 0.80;
+        case 224: return 0.77;
+        case 192: return 0.72;
+        case 128: return 0.50;
+        case 64: return 0.27;
+        default: return 0.15;
     }
 }
 
-void apply_override(KernelConfig& c) {
+struct Choice {
+    int swap, pair, bn;
+    double score;
+};
+
+void apply_override(KernelConfig& c, bool& forced_bn, bool& forced_pair, bool& forced_swap) {
     const char* env = std::getenv("TG_FORCE_CONFIG");
     if (!env || !*env) return;
     char buf[256];
     std::snprintf(buf, sizeof(buf), "%s", env);
     for (char* tok = std::strtok(buf, ", "); tok; tok = std::strtok(nullptr, ", ")) {
         int v = 0;
-        if (std::sscanf(tok, "bn=%d", &v) == 1 && (v == 32 || v == 64 || v == 128 || v == 256))
+        if (std::sscanf(tok, "bn=%d", &v) == 1 && gemm_stages(v, 0) > 0) {
             c.bn = v;
-        else if (std::sscanf(tok, "swap=%d", &v) == 1 && (v == 0 || v == 1))
+            forced_bn = true;
+        } else if (std::sscanf(tok, "swap=%d", &v) == 1 && (v == 0 || v == 1)) {
             c.swap = v;
-        else if (std::sscanf(tok, "group_m=%d", &v) == 1 && v >= 1 && v <= 64)
+            forced_swap = true;
+        } else if (std::sscanf(tok, "pair=%d", &v) == 1 && (v == 0 || v == 1)) {
+            c.pair = v;
+            forced_pair = true;
+        } else if (std::sscanf(tok, "group_m=%d", &v) == 1 && v >= 1 && v <= 64) {
             c.group_m = v;
-        else if (std::sscanf(tok, "grid=%d", &v) == 1 && v >= 1)
+        } else if (std::sscanf(tok, "grid=%d", &v) == 1 && v >= 1) {
             c.grid = v;
+        }
     }
 }
 
@@ -51,43 +78,59 @@ void apply_override(KernelConfig& c) {
 KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int permA, int permB,
                            bool /*has_epilogue*/, int sms) {
     KernelConfig c{};
-    // Operand swap: when M cannot fill the 128 accumulator lanes but N can,
-    // compute C^T = B^T A^T so that N runs along the lanes.
-    c.swap = (M <= 64 && N > M) ? 1 : 0;
-    c.bm = 128;
-    c.pair = 0;
     c.group_m = 8;
-    c.grid = 0;
-    apply_override(c);
-    const int forced_bn = c.bn;
+    bool forced_bn = false, forced_pair = false, forced_swap = false;
+    apply_override(c, forced_bn, forced_pair, forced_swap);
 
-    const int64_t Mk = c.swap ? N : M, Nk = c.swap ? M : N;
-    // Q (the kernel's column operand) is MN-major when its storage runs along
-    // the kernel's columns; such tiles are fetched in 64-column swizzle atoms.
-    const bool q_mn = c.swap ? (permA == 1) : (permB == 0);
-    if (!forced_bn) {
-        double best = -1.0;
-        for (int bn : {256, 128, 64, 32}) {
-            if (bn == 32 && q_mn) continue;
-            const int64_t tiles = cdiv(Mk, 128) * cdiv(Nk, bn);
-            const int64_t waves = cdiv(tiles, sms);
-            const double util = (double)Mk * (double)Nk / ((double)waves * sms * 128.0 * bn);
-            const double score = util * tile_efficiency(bn);
-            if (score > best + 1e-9) {
-                best = score;
-                c.bn = bn;
+    Choice best{0, 0, 0, -1.0};
+    for (int swap = 0; swap < 2; ++swap) {
+        if (forced_swap && swap != c.swap) continue;
+        const int64_t Mk = swap ? N : M, Nk = swap ? M : N;
+        // Q (the kernel's column operand) is MN-major when its storage runs
+        // along the kernel's columns; such tiles are fetched in 64-column atoms.
+        const bool q_mn = swap ? (permA == 1) : (permB == 0);
+        for (int pair = 0; pair < 2; ++pair) {
+            if (forced_pair && pair != c.pair) continue;
+            for (int bn : {256, 224, 192, 128, 64, 32}) {
+                if (forced_bn && bn != c.bn) continue;
+                if (gemm_stages(bn, pair) <= 0) continue;
+                if (bn == 32 && q_mn) continue;  // MN-major atoms are 64 columns wide
+                const int bm = pair ? 256 : 128;
+                const int slots = pair ? sms / 2 : sms;
+                const int64_t tiles = cdiv(Mk, bm) * cdiv(Nk, bn);
+                const int64_t waves = cdiv(tiles, slots);
+                double score = (double)Mk * (double)Nk / ((double)waves * slots * bm * bn) *
+                               tile_efficiency(bn, pair);
+                // A one-tile-wide problem is bandwidth bound: the narrowest tile
+                // that covers it streams the other operand once per SM.
+                if (Nk <= 32 && bn == 32 && !pair) score = 2.0;
+                // The transposed output path stores 2-byte elements per lane:
+                // take it only for a clear gain (or when M cannot fill a tile).
+                if (swap && !(M <= 64 && N > M)) score *= 0.97;
+                if (!swap && M <= 64 && N > M) score *= 0.5;
+                if (score > best.score + 1e-9) best = Choice{swap, pair, bn, score};
             }
         }
-    } else if (forced_bn == 32 && q_mn) {
-        c.bn = 64;
     }
-    const int64_t tiles_m = cdiv(Mk, 128);
+    if (best.score < 0) {  // an impossible forced combination: fall back to the plain default
+        best = Choice{0, 0, 128, 0.0};
+    }
+    c.swap = best.swap;
+    c.pair = best.pair;
+    c.bn = best.bn;
+    c.bm = c.pair ? 256 : 128;
+    const int64_t Mk = c.swap ? N : M, Nk = c.swap ? M : N;
+    const int64_t tiles_m = cdiv(Mk, c.bm);
     const int64_t tiles = tiles_m * cdiv(Nk, c.bn);
     c.tiles = (int)tiles;
     if (c.group_m > tiles_m) c.group_m = (int)tiles_m;
-    if (c.grid <= 0 || c.grid > sms) c.grid = sms;
-    if (c.grid > tiles) c.grid = (int)tiles;
-    c.stages = gemm_stages(c.bn);
+    const int slots = c.pair ? sms / 2 : sms;
+    int clusters = c.grid > 0 ? (c.pair ? c.grid / 2 : c.grid) : slots;
+    if (clusters > slots) clusters = slots;
+    if (clusters > tiles) clusters = (int)tiles;
+    if (clusters < 1) clusters = 1;
+    c.grid = c.pair ? 2 * clusters : clusters;
+    c.stages = gemm_stages(c.bn, c.pair);
     (void)K;
     return c;
 }
