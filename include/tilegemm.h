@@ -112,6 +112,12 @@ const char* tg_status_string(int status);
 int tg_query_config(int64_t M, int64_t N, int64_t K, tg_dtype dtype, tg_perm permA,
                     tg_perm permB, const tg_epilogue* epi, char* buf, size_t len);
 
+/* tg_query_config for a device with `sms` SMs (2..4096), without touching
+ * any device: the selector's host logic alone. */
+int tg_query_config_for_sms(int sms, int64_t M, int64_t N, int64_t K, tg_dtype dtype,
+                            tg_perm permA, tg_perm permB, const tg_epilogue* epi, char* buf,
+                            size_t len);
+
 /*
  * Reads and clears the device status word of the current device: TG_OK, or
  * TG_ERR_TIMEOUT if some earlier kernel's bounded wait expired (the kernel

@@ -59,6 +59,8 @@ _sig("tg_gemm", _int, _i64, _i64, _i64, _vp, _i64, _int, _vp, _i64, _int, _vp, _
 _sig("tg_status_string", _cp, _int)
 _sig("tg_query_config", _int, _i64, _i64, _i64, _int, _int, _int, ctypes.POINTER(tg_epilogue),
      ctypes.c_char_p, ctypes.c_size_t)
+_sig("tg_query_config_for_sms", _int, _int, _i64, _i64, _i64, _int, _int, _int,
+     ctypes.POINTER(tg_epilogue), ctypes.c_char_p, ctypes.c_size_t)
 _sig("tg_debug_status", _int, ctypes.POINTER(_int))
 _sig("tg_debug_configure", _int, _i64, _i64)
 _sig("tg_probe_swizzle128", _int, _vp, _int, _i64, _vp, _vp, _vp)
@@ -89,7 +91,8 @@ _sig("tg_layout_swizzle128", _int, _int, _int, _PP)
 _sig("tg_layout_tmem_32x32b", _int, _int, _PP)
 
 EXPORTED = [
-    "tg_gemm", "tg_status_string", "tg_query_config", "tg_debug_status", "tg_debug_configure",
+    "tg_gemm", "tg_status_string", "tg_query_config", "tg_query_config_for_sms",
+    "tg_debug_status", "tg_debug_configure",
     "tg_probe_swizzle128", "tg_probe_tmem_32x32b", "tg_layout_create", "tg_layout_destroy",
     "tg_layout_num_dims", "tg_layout_in_dim", "tg_layout_out_dim", "tg_layout_get_bases",
     "tg_layout_apply", "tg_layout_compose", "tg_layout_product", "tg_layout_sublayout",
@@ -152,6 +155,16 @@ def tg_query_config(M, N, K, dtype, permA=TG_OP_N, permB=TG_OP_N, epi=None) -> s
                               ctypes.byref(epi) if epi is not None else None, buf, len(buf))
     if rc != TG_OK:
         raise TileGemmError(rc, "tg_query_config")
+    return buf.value.decode()
+
+
+def tg_query_config_for_sms(sms, M, N, K, dtype, permA=TG_OP_N, permB=TG_OP_N, epi=None) -> str:
+    buf = ctypes.create_string_buffer(256)
+    rc = _lib.tg_query_config_for_sms(sms, M, N, K, dtype, permA, permB,
+                                      ctypes.byref(epi) if epi is not None else None, buf,
+                                      len(buf))
+    if rc != TG_OK:
+        raise TileGemmError(rc, "tg_query_config_for_sms")
     return buf.value.decode()
 
 

@@ -381,6 +381,20 @@ extern "C" int tg_query_config(int64_t M, int64_t N, int64_t K, tg_dtype dtype, 
     return TG_OK;
 }
 
+extern "C" int tg_query_config_for_sms(int sms, int64_t M, int64_t N, int64_t K, tg_dtype dtype,
+                                       tg_perm permA, tg_perm permB, const tg_epilogue* epi,
+                                       char* buf, size_t len) {
+    int rc = check_shape(M, N, K, (int)dtype, (int)permA, (int)permB, epi);
+    if (rc) return rc;
+    if (!buf || sms < 2 || sms > 4096) return TG_ERR_INVALID_ARG;
+    const bool has_epi = epi && (epi->bias_n || epi->scale_m || epi->residual || epi->relu);
+    const KernelConfig c = select_config(M, N, K, (int)dtype, (int)permA, (int)permB, has_epi, sms);
+    const std::string s = describe_config(c);
+    if (s.size() + 1 > len) return TG_ERR_BUFFER;
+    std::memcpy(buf, s.c_str(), s.size() + 1);
+    return TG_OK;
+}
+
 extern "C" int tg_debug_status(int* detail) {
     int dev;
     DeviceInfo* info;

@@ -17,31 +17,35 @@ namespace {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Relative tensor-pipe efficiency of a tile shape in steady state.  A
-// single-CTA 128 x BN tile stages 16 KB of A and BN*128 bytes of B per 64-deep
-// K block, and the tensor core reads the same bytes back: narrower tiles move
-// more shared-memory bytes per flop and stall on shared-memory bandwidth.  A
-// CTA pair (256 x BN on two SMs) halves the B bytes each SM stages.  Values
-// are calibrated on GB300 measurements of this kernel (4096^3 and
-// 8192 x 8192 x 4096 sweeps over every compiled tile).
-double tile_efficiency(int bn, int pair) {
+// Relative tensor-pipe efficiency of a tile in steady state, indexed by the
+// B columns it stages.  A single-CTA 128 x BN tile stages 16 KB of A and
+// BN*128 bytes of B per 64-deep K block and the tensor core reads the same
+// bytes back, so narrower tiles move more shared-memory bytes per flop and
+// stall on shared-memory bandwidth; a CTA pair (256 x BN on two SMs) halves
+// the B bytes each SM stages.  Calibrated on GB300 sweeps of this kernel over
+// every compiled tile at 4096^3 and 8192 x 8192 x 4096 (fp16, row-major).
+double tile_efficiency(int cols, int pair) {
     if (pair) {
-        switch (bn) {
-            case 256: return 0.90;
-            case 224: return 0.88;
-            case 192: return 0.84;
-            case 128: return 0.72;
-            default: return 0.5;
-        }
+        if (cols >= 256) return 0.88;
+        if (cols >= 224) return 0.83;
+        if (cols >= 192) return 0.75;
+        if (cols >= 128) return 0.49;
+        return 0.3;
     }
-    switch (bn) {
-        case 256: return 0.80;
-        case 224: return 0.77;
-        case 192: return 0.72;
-        case 128: return 0.50;
-        case 64: return 0.27;
-        default: return 0.15;
-    }
+    if (cols >= 256) return 0.79;
+    if (cols >= 224) return 0.74;
+    if (cols >= 192) return 0.675;
+    if (cols >= 128) return 0.49;
+    if (cols >= 64) return 0.26;
+    return 0.15;
+}
+
+// B columns a tile actually stages: MN-major B arrives in whole 64-column
+// swizzle atoms per CTA.
+int staged_columns(int bn, int pair, bool q_mn) {
+    if (!q_mn) return bn;
+    const int per_cta = pair ? bn / 2 : bn;
+    return ((per_cta + 63) / 64) * 64 * (pair ? 2 : 1);
 }
 
 struct Choice {
@@ -99,15 +103,17 @@ KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int p
                 const int slots = pair ? sms / 2 : sms;
                 const int64_t tiles = cdiv(Mk, bm) * cdiv(Nk, bn);
                 const int64_t waves = cdiv(tiles, slots);
-                double score = (double)Mk * (double)Nk / ((double)waves * slots * bm * bn) *
-                               tile_efficiency(bn, pair);
+                const int cols = staged_columns(bn, pair, q_mn);
+                double score = (double)Mk * (double)Nk / ((double)waves * slots * bm * cols) *
+                               tile_efficiency(cols, pair);
                 // A one-tile-wide problem is bandwidth bound: the narrowest tile
                 // that covers it streams the other operand once per SM.
                 if (Nk <= 32 && bn == 32 && !pair) score = 2.0;
-                // The transposed output path stores 2-byte elements per lane:
-                // take it only for a clear gain (or when M cannot fill a tile).
-                if (swap && !(M <= 64 && N > M)) score *= 0.97;
-                if (!swap && M <= 64 && N > M) score *= 0.5;
+                // Swapping pays only when M cannot fill the 128 accumulator
+                // lanes: the transposed output path stores one 2-byte element
+                // per lane and measured 12% slower at 4096^3.
+                const bool small_m = M <= 64 && N > M;
+                if (swap != (small_m ? 1 : 0) && !forced_swap) continue;
                 if (score > best.score + 1e-9) best = Choice{swap, pair, bn, score};
             }
         }
