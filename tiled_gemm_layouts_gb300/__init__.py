@@ -14,7 +14,9 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libtilegemm.so")
+# TILEGEMM_LIBRARY selects another build of the same library (e.g. one built
+# with different flags); the default is the in-tree build.
+LIB_PATH = os.environ.get("TILEGEMM_LIBRARY") or os.path.join(_HERE, "libtilegemm.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(

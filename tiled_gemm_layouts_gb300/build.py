@@ -19,8 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtilegemm.so")
 
-CUDA_SOURCES = ["api.cu", "gemm_sm103.cu", "gemm_inst_a.cu", "gemm_inst_b.cu", "gemm_inst_c.cu",
-                "gemm_inst_d.cu", "probes.cu"]
+CUDA_SOURCES = ["api.cu", "gemm_sm103.cu", "probes.cu"] + [f"gemm_inst_{i}.cu" for i in range(1, 13)]
 CXX_SOURCES = ["layout.cpp", "select.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1,0 +1,7 @@
+// gemm_inst_7.cu -- explicit instantiations of some tile configurations.
+#include "gemm_launch.cuh"
+
+namespace tg {
+TG_INSTANTIATE(128, true, false)
+TG_INSTANTIATE(192, true, false)
+}  // namespace tg

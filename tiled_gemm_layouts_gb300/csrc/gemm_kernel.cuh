@@ -126,8 +126,76 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8], int bf16)
     }
 }
 
+// Residual and bias values of one full 32-column run of row m, loaded ahead
+// of the accumulator so that their latency overlaps the TMEM read.
+struct Aux {
+    uint4 r[4];
+    uint4 b[4];
+};
+
+// Issues the loads for the run C(m, c0 .. c0+31) if it is full and inside C;
+// returns whether it is (otherwise the chunk takes the masked scalar path).
+__device__ __forceinline__ bool prefetch_aux(const GemmParams& p, int m, int c0, Aux& a) {
+    if (p.swap || m >= p.M || c0 + 32 > p.N) return false;
+    if (p.resid) {
+        const uint4* r = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.resid) +
+                                                        (long long)m * p.ldr + c0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) a.r[v] = __ldg(r + v);
+    }
+    if (p.bias_n) {
+        const uint4* b = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.bias_n) + c0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) a.b[v] = __ldg(b + v);
+    }
+    return true;
+}
+
+// Epilogue of a full run C(m, c0 .. c0+31) with its operands already loaded.
+__device__ __forceinline__ void epilogue_run(const GemmParams& p, int m, int c0, float (&y)[32],
+                                             float row_scale, const Aux& a) {
+    const int bf = p.bf16;
+    if (p.scale_m) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] *= row_scale;
+    }
+    if (p.bias_n) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            float f[8];
+            unpack8(a.b[v], f, bf);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[8 * v + i] += f[i];
+        }
+    }
+    if (p.relu) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] = fmaxf(y[j], 0.0f);
+    }
+    if (p.resid) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            float f[8];
+            unpack8(a.r[v], f, bf);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[8 * v + i] += f[i];
+        }
+    }
+    uint4* c = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.C) + (long long)m * p.ldc + c0);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        uint4 u;
+        u.x = pack2(y[8 * v + 0], y[8 * v + 1], bf);
+        u.y = pack2(y[8 * v + 2], y[8 * v + 3], bf);
+        u.z = pack2(y[8 * v + 4], y[8 * v + 5], bf);
+        u.w = pack2(y[8 * v + 6], y[8 * v + 7], bf);
+        c[v] = u;
+    }
+}
+
 // Epilogue for one 32-column chunk held by this thread: kernel row `rk`
-// (one TMEM lane), kernel columns c0 .. c0+31 in y[].
+// (one TMEM lane), kernel columns c0 .. c0+31 in y[].  General path: edge
+// runs of C, and the swapped (transposed-output) layout.
 __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int rk, int c0,
                                                float (&y)[32], float row_scale, float row_bias) {
     const int bf = p.bf16;
@@ -212,7 +280,10 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int rk, int 
     }
 }
 
-template <int BN, bool PAIR>
+// AUX = true: the epilogue reads a bias and/or residual; their loads are
+// issued one 32-column run ahead (and before the accumulator is ready).
+// AUX = false keeps the plain epilogue lean.
+template <int BN, bool PAIR, bool AUX>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
     using TS = TileShape<BN, PAIR>;
     constexpr int STAGES = TS::kStages;
@@ -409,14 +480,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         for (int t = cta_tile0; t < p.num_tiles; t += tile_step, ++i) {
             const int buf = i & 1;
             const uint32_t aph = (i >> 1) & 1;
+            int tm, tn;
+            tile_coords(p, t, tm, tn);
+            const int rk = tm * TS::kBM + (int)rank * 128 + q * 32 + lane;
+            // operands of the first run do not depend on the accumulator:
+            // fetch them while the main loop still runs
+            Aux cur, nxt;
+            bool cur_full = AUX ? prefetch_aux(p, rk, tn * BN, cur) : false;
             int ok = 1;
             if (lane == 0) ok = wait_bar(smem_addr(&tfull[buf]), aph, w, DEV_TIMEOUT_EPILOGUE);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            int tm, tn;
-            tile_coords(p, t, tm, tn);
-            const int rk = tm * TS::kBM + (int)rank * 128 + q * 32 + lane;
             float row_scale = 1.0f, row_bias = 0.0f;
             if (!p.swap) {
                 if (p.scale_m && rk < p.M) row_scale = to_f32(static_cast<const uint16_t*>(p.scale_m)[rk], p.bf16);
@@ -444,7 +519,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 float y[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(v[j]);
-                epilogue_chunk(p, rk, tn * BN + c * 32, y, row_scale, row_bias);
+                if constexpr (AUX) {
+                    bool nxt_full = false;
+                    if (c + 1 < BN / 32)
+                        nxt_full = prefetch_aux(p, rk, tn * BN + (c + 1) * 32, nxt);
+                    if (cur_full)
+                        epilogue_run(p, rk, tn * BN + c * 32, y, row_scale, cur);
+                    else
+                        epilogue_chunk(p, rk, tn * BN + c * 32, y, row_scale, row_bias);
+                    cur = nxt;
+                    cur_full = nxt_full;
+                } else {
+                    epilogue_chunk(p, rk, tn * BN + c * 32, y, row_scale, row_bias);
+                }
             }
         }
     }
