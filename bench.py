@@ -211,7 +211,9 @@ def algorithmic_bytes(p) -> int:
 
 
 class DeviceProblem:
-    def __init__(self, tg, p):
+    """Device-resident inputs, output and (for tg_gemm_ws) a zeroed workspace."""
+
+    def __init__(self, tg, p, stream_k=True):
         import numpy as np
         import torch
         self.p = p
@@ -223,11 +225,18 @@ class DeviceProblem:
         self.C = torch.empty((p["M"], p["N"]), dtype=torch.int16, device="cuda")
         self.epi = tg.make_epilogue(self.bias, self.scale, p.get("relu", False), self.R,
                                     p.get("ldr", 0) or 0)
+        self.ws_bytes = tg.tg_gemm_workspace_size(p["M"], p["N"], p["K"], p["dtype"], p["permA"],
+                                                  p["permB"], self.epi) if stream_k else 0
+        self.ws = (torch.zeros(self.ws_bytes, dtype=torch.uint8, device="cuda")
+                   if self.ws_bytes else None)
+        self.config = (tg.tg_query_config_ws if stream_k else tg.tg_query_config)(
+            p["M"], p["N"], p["K"], p["dtype"], p["permA"], p["permB"], self.epi)
 
     def call(self, stream):
         p = self.p
-        self.tg.gemm(p["M"], p["N"], p["K"], self.A, p["lda"], p["permA"], self.B, p["ldb"],
-                     p["permB"], self.C, p["N"], p["dtype"], self.epi, stream)
+        self.tg.gemm_ws(p["M"], p["N"], p["K"], self.A, p["lda"], p["permA"], self.B, p["ldb"],
+                        p["permB"], self.C, p["N"], p["dtype"], self.epi, self.ws, self.ws_bytes,
+                        stream)
 
 
 def time_kernel(fn, steps, warmup, flush_buf, stream):
@@ -304,6 +313,8 @@ def main():
                     help="skip the other workloads and the CPU baseline (for profiling)")
     ap.add_argument("--workload", default="fp16_4096", help="headline workload key")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-stream-k", action="store_true",
+                    help="call tg_gemm (whole tiles only) instead of tg_gemm_ws")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -329,7 +340,7 @@ def main():
 
     # ---------------- headline: device-resident inputs
     hp = make_problem(specs[args.workload])
-    prob = DeviceProblem(tg, hp)
+    prob = DeviceProblem(tg, hp, stream_k=not args.no_stream_k)
     M, N, K = hp["M"], hp["N"], hp["K"]
     flops = 2.0 * M * N * K
     barrier(world)
@@ -370,8 +381,8 @@ def main():
             for k, h in host_in.items():
                 if h is not None:
                     dev_in[k].copy_(h, non_blocking=True)
-            tg.gemm(M, N, K, dev_in["A"], hp["lda"], hp["permA"], dev_in["B"], hp["ldb"],
-                    hp["permB"], dC, N, hp["dtype"], e2e_epi, s)
+            tg.gemm_ws(M, N, K, dev_in["A"], hp["lda"], hp["permA"], dev_in["B"], hp["ldb"],
+                       hp["permB"], dC, N, hp["dtype"], e2e_epi, prob.ws, prob.ws_bytes, s)
             hC.copy_(dC, non_blocking=True)
 
     e2e_times = time_kernel(e2e_step, max(5, args.steps // 2), 3, flush, stream)
@@ -388,7 +399,8 @@ def main():
         "data": "synthetic (SplitMix64 seed 1002, uniform[-1,1] rounded to fp16)",
         "config": {"workload": HEADLINE, "M": M, "N": N, "K": K, "layout": "row-major A, B, C",
                    "accumulate": "fp32", "l2": "flushed before every step (512 MB write)",
-                   "tile": tg.tg_query_config(M, N, K, hp["dtype"], hp["permA"], hp["permB"]),
+                   "tile": prob.config, "api": "tg_gemm_ws" if prob.ws_bytes else "tg_gemm",
+                   "workspace_bytes": prob.ws_bytes,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "pct_dense_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -411,14 +423,13 @@ def main():
                     "fp16_4000x3000x1000_strided", "bf16_16384x1024x8192_scale",
                     "bf16_32x16384x16384_scale"):
             p = make_problem(specs[key])
-            dp = DeviceProblem(tg, p)
+            dp = DeviceProblem(tg, p, stream_k=not args.no_stream_k)
             ts = time_kernel(dp.call, 10, 3, flush, stream)
             t = statistics.median(ts) * 1e-3
             f = 2.0 * p["M"] * p["N"] * p["K"]
             entry = {"tflops": f / t / 1e12, "pct_dense_peak": 100 * f / t / 1e12 / peak,
                      "ms_median": t * 1e3,
-                     "tile": tg.tg_query_config(p["M"], p["N"], p["K"], p["dtype"], p["permA"],
-                                                p["permB"], dp.epi)}
+                     "tile": dp.config}
             if key.startswith("bf16_32x"):
                 gbs = algorithmic_bytes(p) / t / 1e9
                 entry.update({"gbs": gbs, "hbm_frac": gbs / float(peaks.get("hbm_gbs", 6800.0))})

@@ -96,6 +96,37 @@ int tg_gemm(int64_t M, int64_t N, int64_t K,
             void* C, int64_t ldc, tg_dtype dtype,
             const tg_epilogue* epi, cudaStream_t stream);
 
+/*
+ * tg_gemm with a caller-provided workspace that lets the kernel deal the
+ * tiles of its last waves out as equal K-ranges over all SMs ("stream-K"):
+ * when the tile count is not a multiple of the number of persistent workers,
+ * the tail would otherwise leave SMs idle.  A tile whose K-range is split
+ * is finished by the contributor that arrives last, which adds the fp32
+ * partial sums in K order (results are reproducible call to call); no CTA
+ * ever waits for another.
+ *
+ * workspace: device memory of the current device, 256-byte aligned, at least
+ *   tg_gemm_workspace_size() bytes, disjoint from every operand, filled with
+ *   zero bytes before its first use (e.g. cudaMemset once); every completed
+ *   call leaves its counters at zero again.  After TG_ERR_TIMEOUT from
+ *   tg_debug_status, zero it again.  Calls that share a workspace must not
+ *   run concurrently on the GPU.
+ * workspace == NULL: exactly tg_gemm.  Other arguments, checks and errors as
+ * tg_gemm; TG_ERR_BUFFER if workspace_bytes is too small, TG_ERR_ALIGN /
+ * TG_ERR_OVERLAP / TG_ERR_POINTER for a misplaced workspace.
+ */
+int tg_gemm_ws(int64_t M, int64_t N, int64_t K,
+               const void* A, int64_t lda, tg_perm permA,
+               const void* B, int64_t ldb, tg_perm permB,
+               void* C, int64_t ldc, tg_dtype dtype,
+               const tg_epilogue* epi, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream);
+
+/* Workspace bytes tg_gemm_ws needs for these arguments on the current device
+ * (0 when every tile is computed whole). */
+int tg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, tg_dtype dtype, tg_perm permA,
+                           tg_perm permB, const tg_epilogue* epi, size_t* bytes);
+
 /* Static name of a status code ("TG_OK", "TG_ERR_ALIGN", ...). */
 const char* tg_status_string(int status);
 
@@ -112,11 +143,16 @@ const char* tg_status_string(int status);
 int tg_query_config(int64_t M, int64_t N, int64_t K, tg_dtype dtype, tg_perm permA,
                     tg_perm permB, const tg_epilogue* epi, char* buf, size_t len);
 
-/* tg_query_config for a device with `sms` SMs (2..4096), without touching
- * any device: the selector's host logic alone. */
-int tg_query_config_for_sms(int sms, int64_t M, int64_t N, int64_t K, tg_dtype dtype,
-                            tg_perm permA, tg_perm permB, const tg_epilogue* epi, char* buf,
-                            size_t len);
+/* The configuration tg_gemm_ws would use (adds sk_tiles, sk_cmax, ws_bytes). */
+int tg_query_config_ws(int64_t M, int64_t N, int64_t K, tg_dtype dtype, tg_perm permA,
+                       tg_perm permB, const tg_epilogue* epi, char* buf, size_t len);
+
+/* tg_query_config (stream_k = 0) or tg_query_config_ws (stream_k = 1) for a
+ * device with `sms` SMs (2..4096), without touching any device: the
+ * selector's host logic alone. */
+int tg_query_config_for_sms(int sms, int stream_k, int64_t M, int64_t N, int64_t K,
+                            tg_dtype dtype, tg_perm permA, tg_perm permB, const tg_epilogue* epi,
+                            char* buf, size_t len);
 
 /*
  * Reads and clears the device status word of the current device: TG_OK, or

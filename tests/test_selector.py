@@ -69,3 +69,91 @@ def test_rejects_bad_shape(tg):
         tg.tg_query_config_for_sms(152, 0, 1, 1, F16)
     with pytest.raises(tg.TileGemmError):
         tg.tg_query_config_for_sms(1, 16, 16, 16, F16)
+
+
+def test_stream_k_split(tg):
+    # 256 pair tiles over 76 clusters: 2 whole waves, then 76 + 28 tiles dealt out in K-ranges
+    c = cfg_sk(tg, 4096, 4096, 4096, F16, 0, 0)
+    assert (c["pair"], c["bn"], c["grid"], c["tiles"], c["sk_tiles"]) == (1, 256, 152, 256, 104)
+    assert c["sk_cmax"] == 2
+    counters = -(-(76 * 2 * 4) // 256) * 256
+    assert c["ws_bytes"] == counters + 76 * 2 * 256 * 256 * 4
+    # whole waves: nothing to split
+    c = cfg_sk(tg, 256 * 76 // 4, 1024, 4096, F16, 0, 0)  # 19 x 4 = 76 tiles
+    assert c["sk_tiles"] == 0 and c["ws_bytes"] == 0
+    # fewer tiles than SMs: every tile is shared (up to 3 contributors)
+    c = cfg_sk(tg, 32, 16384, 16384, BF16, 0, 0)
+    assert (c["sk_tiles"], c["grid"], c["sk_cmax"]) == (128, 152, 3)
+    # without a workspace the same shapes keep whole tiles
+    assert cfg(tg, 4096, 4096, 4096, F16, 0, 0)["sk_tiles"] == 0
+
+
+def cfg_sk(tg, *args, sms=152):
+    return tg.parse_config(tg.tg_query_config_for_sms(sms, *args, stream_k=True))
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_stream_k_invariants(tg, seed):
+    rng = np.random.default_rng(1000 + seed)
+    M, N, K = (int(x) for x in rng.integers(1, 30000, 3))
+    sms = int(rng.choice([8, 64, 148, 152]))
+    c = cfg_sk(tg, M, N, K, BF16, 0, 1, sms=sms)
+    workers = c["grid"] // 2 if c["pair"] else c["grid"]
+    kb = -(-K // 64)
+    if c["sk_tiles"]:
+        assert c["sk_tiles"] <= c["tiles"]
+        assert c["tiles"] % workers != 0
+        assert c["sk_tiles"] * kb >= 2 * workers
+        shortest = c["sk_tiles"] * kb // workers
+        # a tile's K-range never meets more ranges than there are slots
+        assert c["sk_cmax"] >= (kb - 1) // shortest + 2 or c["sk_cmax"] == workers
+        assert c["ws_bytes"] >= workers * c["sk_cmax"] * c["bm"] * c["bn"] * 4
+    else:
+        assert c["ws_bytes"] == 0
+
+
+def simulate_items(workers, dp_tiles, sk_tiles, kb):
+    """The kernel's work split, restated: whole tiles w, w+workers, ... below
+    dp_tiles, then equal contiguous ranges of the sk_tiles*kb iterations."""
+    iters = sk_tiles * kb
+    items = {}
+    for w in range(workers):
+        out = [(t, 0, kb) for t in range(w, dp_tiles, workers)]
+        it, end = iters * w // workers, iters * (w + 1) // workers
+        while it < end:
+            ts = it // kb
+            k0 = it - ts * kb
+            k1 = min(kb, k0 + (end - it))
+            out.append((dp_tiles + ts, k0, k1))
+            it += k1 - k0
+        items[w] = out
+    return items
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_stream_k_schedule_covers_every_k_block_once(tg, seed):
+    rng = np.random.default_rng(2000 + seed)
+    M, N, K = (int(x) for x in rng.integers(1, 20000, 3))
+    sms = int(rng.choice([8, 16, 64, 152]))
+    c = cfg_sk(tg, M, N, K, F16, 1, 0, sms=sms)
+    workers = c["grid"] // 2 if c["pair"] else c["grid"]
+    kb = -(-K // 64)
+    dp = c["tiles"] - c["sk_tiles"]
+    items = simulate_items(workers, dp, c["sk_tiles"], kb)
+    seen = {}
+    owners = {}
+    for w, its in items.items():
+        for t, k0, k1 in its:
+            assert 0 <= k0 < k1 <= kb and 0 <= t < c["tiles"]
+            for k in range(k0, k1):
+                assert (t, k) not in seen
+                seen[(t, k)] = w
+            owners.setdefault(t, []).append(w)
+    assert len(seen) == c["tiles"] * kb
+    first_owners = set()
+    for t, ws in owners.items():
+        assert ws == sorted(ws) and ws == list(range(ws[0], ws[0] + len(ws)))
+        if len(ws) > 1:  # a split tile: its slots and counter are indexed by the first owner
+            assert len(ws) <= c["sk_cmax"]
+            assert ws[0] not in first_owners
+            first_owners.add(ws[0])

@@ -61,8 +61,14 @@ _sig("tg_gemm", _int, _i64, _i64, _i64, _vp, _i64, _int, _vp, _i64, _int, _vp, _
 _sig("tg_status_string", _cp, _int)
 _sig("tg_query_config", _int, _i64, _i64, _i64, _int, _int, _int, ctypes.POINTER(tg_epilogue),
      ctypes.c_char_p, ctypes.c_size_t)
-_sig("tg_query_config_for_sms", _int, _int, _i64, _i64, _i64, _int, _int, _int,
+_sig("tg_query_config_for_sms", _int, _int, _int, _i64, _i64, _i64, _int, _int, _int,
      ctypes.POINTER(tg_epilogue), ctypes.c_char_p, ctypes.c_size_t)
+_sig("tg_query_config_ws", _int, _i64, _i64, _i64, _int, _int, _int, ctypes.POINTER(tg_epilogue),
+     ctypes.c_char_p, ctypes.c_size_t)
+_sig("tg_gemm_ws", _int, _i64, _i64, _i64, _vp, _i64, _int, _vp, _i64, _int, _vp, _i64, _int,
+     ctypes.POINTER(tg_epilogue), _vp, ctypes.c_size_t, _vp)
+_sig("tg_gemm_workspace_size", _int, _i64, _i64, _i64, _int, _int, _int,
+     ctypes.POINTER(tg_epilogue), ctypes.POINTER(ctypes.c_size_t))
 _sig("tg_debug_status", _int, ctypes.POINTER(_int))
 _sig("tg_debug_configure", _int, _i64, _i64)
 _sig("tg_probe_swizzle128", _int, _vp, _int, _i64, _vp, _vp, _vp)
@@ -93,7 +99,8 @@ _sig("tg_layout_swizzle128", _int, _int, _int, _PP)
 _sig("tg_layout_tmem_32x32b", _int, _int, _PP)
 
 EXPORTED = [
-    "tg_gemm", "tg_status_string", "tg_query_config", "tg_query_config_for_sms",
+    "tg_gemm", "tg_gemm_ws", "tg_gemm_workspace_size", "tg_status_string", "tg_query_config",
+    "tg_query_config_ws", "tg_query_config_for_sms",
     "tg_debug_status", "tg_debug_configure",
     "tg_probe_swizzle128", "tg_probe_tmem_32x32b", "tg_layout_create", "tg_layout_destroy",
     "tg_layout_num_dims", "tg_layout_in_dim", "tg_layout_out_dim", "tg_layout_get_bases",
@@ -151,6 +158,41 @@ def gemm(M, N, K, A, lda, permA, B, ldb, permB, C, ldc, dtype, epi=None, stream=
         raise TileGemmError(rc, "tg_gemm")
 
 
+def tg_gemm_ws(M, N, K, A, lda, permA, B, ldb, permB, C, ldc, dtype, epi, workspace,
+               workspace_bytes, stream=None) -> int:
+    """Status of one tg_gemm_ws call; never raises."""
+    return _lib.tg_gemm_ws(M, N, K, _addr(A), lda, permA, _addr(B), ldb, permB, _addr(C), ldc,
+                           dtype, ctypes.byref(epi) if epi is not None else None,
+                           _addr(workspace), workspace_bytes, _stream(stream))
+
+
+def gemm_ws(M, N, K, A, lda, permA, B, ldb, permB, C, ldc, dtype, epi, workspace,
+            workspace_bytes, stream=None) -> None:
+    rc = tg_gemm_ws(M, N, K, A, lda, permA, B, ldb, permB, C, ldc, dtype, epi, workspace,
+                    workspace_bytes, stream)
+    if rc != TG_OK:
+        raise TileGemmError(rc, "tg_gemm_ws")
+
+
+def tg_gemm_workspace_size(M, N, K, dtype, permA=TG_OP_N, permB=TG_OP_N, epi=None) -> int:
+    n = ctypes.c_size_t(0)
+    rc = _lib.tg_gemm_workspace_size(M, N, K, dtype, permA, permB,
+                                     ctypes.byref(epi) if epi is not None else None,
+                                     ctypes.byref(n))
+    if rc != TG_OK:
+        raise TileGemmError(rc, "tg_gemm_workspace_size")
+    return n.value
+
+
+def tg_query_config_ws(M, N, K, dtype, permA=TG_OP_N, permB=TG_OP_N, epi=None) -> str:
+    buf = ctypes.create_string_buffer(256)
+    rc = _lib.tg_query_config_ws(M, N, K, dtype, permA, permB,
+                                 ctypes.byref(epi) if epi is not None else None, buf, len(buf))
+    if rc != TG_OK:
+        raise TileGemmError(rc, "tg_query_config_ws")
+    return buf.value.decode()
+
+
 def tg_query_config(M, N, K, dtype, permA=TG_OP_N, permB=TG_OP_N, epi=None) -> str:
     buf = ctypes.create_string_buffer(256)
     rc = _lib.tg_query_config(M, N, K, dtype, permA, permB,
@@ -160,9 +202,10 @@ def tg_query_config(M, N, K, dtype, permA=TG_OP_N, permB=TG_OP_N, epi=None) -> s
     return buf.value.decode()
 
 
-def tg_query_config_for_sms(sms, M, N, K, dtype, permA=TG_OP_N, permB=TG_OP_N, epi=None) -> str:
+def tg_query_config_for_sms(sms, M, N, K, dtype, permA=TG_OP_N, permB=TG_OP_N, epi=None,
+                            stream_k=False) -> str:
     buf = ctypes.create_string_buffer(256)
-    rc = _lib.tg_query_config_for_sms(sms, M, N, K, dtype, permA, permB,
+    rc = _lib.tg_query_config_for_sms(sms, int(stream_k), M, N, K, dtype, permA, permB,
                                       ctypes.byref(epi) if epi is not None else None, buf,
                                       len(buf))
     if rc != TG_OK:

@@ -216,7 +216,8 @@ int check_pointers(const Args& a, int dev) {
 }
 
 bool encode_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner, uint64_t outer,
-               int64_t ld, uint32_t box_inner, uint32_t box_outer) {
+               int64_t ld, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
     const cuuint32_t box[2] = {box_inner, box_outer};
@@ -224,8 +225,7 @@ bool encode_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner, ui
     const CUtensorMapDataType dt =
         dtype == TG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     return g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -247,7 +247,7 @@ uint32_t make_idesc(int dtype, bool p_mn, bool q_mn, int n, int m) {
 
 }  // namespace
 
-int gemm_impl(const Args& a, cudaStream_t stream) {
+int gemm_impl(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t stream) {
     int rc = check_shape(a.M, a.N, a.K, a.dtype, a.permA, a.permB, nullptr);
     if (rc) return rc;
     if (a.relu != 0 && a.relu != 1) return TG_ERR_INVALID_ARG;
@@ -262,7 +262,25 @@ int gemm_impl(const Args& a, cudaStream_t stream) {
     const KernelConfig cfg = select_config(a.M, a.N, a.K, a.dtype, a.permA, a.permB,
                                            a.bias != nullptr || a.scale != nullptr ||
                                                a.resid != nullptr || a.relu,
-                                           info->sms);
+                                           info->sms, workspace != nullptr);
+    if (cfg.sk_tiles > 0) {
+        // The workspace is written: it must be device memory of this device,
+        // large enough, and disjoint from every operand.
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TG_ERR_ALIGN;
+        if ((long long)ws_bytes < cfg.ws_bytes) return TG_ERR_BUFFER;
+        Span ws;
+        ws.present = true;
+        ws.lo = reinterpret_cast<uintptr_t>(workspace);
+        ws.hi = (u128)ws.lo + (u128)cfg.ws_bytes;
+        const int64_t a_rows = a.permA == TG_OP_N ? a.M : a.K, a_w = a.permA == TG_OP_N ? a.K : a.M;
+        const int64_t b_rows = a.permB == TG_OP_N ? a.K : a.N, b_w = a.permB == TG_OP_N ? a.N : a.K;
+        const Span others[6] = {span_of(a.C, a.M, a.N, a.ldc), span_of(a.A, a_rows, a_w, a.lda),
+                                span_of(a.B, b_rows, b_w, a.ldb), span_of(a.bias, 1, a.N, a.N),
+                                span_of(a.scale, 1, a.M, a.M), span_of(a.resid, a.M, a.N, a.ldr)};
+        for (const Span& o : others)
+            if (intersects(ws, o)) return TG_ERR_OVERLAP;
+        if ((rc = check_pointer(workspace, ws, dev))) return rc;
+    }
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
     const bool swap = cfg.swap != 0;
@@ -291,6 +309,13 @@ int gemm_impl(const Args& a, cudaStream_t stream) {
         ok = encode_operand(&p.map_p, a.dtype, a.B, a.N, a.K, a.ldb, p_mn, 128) &&
              encode_operand(&p.map_q, a.dtype, a.A, a.M, a.K, a.lda, q_mn, q_box);
     }
+    // C for the epilogue's tensor stores: 32 x 32 chunks, rows of 64 bytes.
+    // A tensor store bounds the innermost dimension in 16-byte units, so the
+    // map stops at N rounded down to 8 columns; the kernel stores the rest
+    // of each row directly (a map of at least 8 columns stays encodable).
+    p.n_tma = (int)(a.N & ~int64_t(7));
+    ok = ok && encode_2d(&p.map_c, a.dtype, a.C, p.n_tma > 0 ? (uint64_t)p.n_tma : 8u, a.M,
+                         a.ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!ok) return TG_ERR_CUDA;
     p.p_mn_major = p_mn;
     p.q_mn_major = q_mn;
@@ -306,6 +331,16 @@ int gemm_impl(const Args& a, cudaStream_t stream) {
     p.resid = a.resid;
     p.ldr = a.ldr;
     p.relu = a.relu;
+    p.workers = cfg.pair ? cfg.grid / 2 : cfg.grid;
+    p.sk_tiles = cfg.sk_tiles;
+    p.dp_tiles = p.num_tiles - cfg.sk_tiles;
+    p.sk_cmax = cfg.sk_cmax;
+    p.sk_iters = (long long)cfg.sk_tiles * p.num_kb;
+    if (cfg.sk_tiles > 0) {
+        const long long counters = ((long long)p.workers * 2 * 4 + 255) / 256 * 256;
+        p.ws_count = static_cast<int*>(workspace);
+        p.ws_partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + counters);
+    }
     p.timeout_cycles = g_timeout.load();
     p.status = info->status;
     p.inject_skip_load = (int)g_skip_kblock.load();
@@ -343,7 +378,48 @@ extern "C" int tg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     a.resid = epi ? epi->residual : nullptr;
     a.ldr = (epi && epi->residual) ? (epi->ldr ? epi->ldr : ldc) : 0;
     a.relu = epi ? epi->relu : 0;
-    return gemm_impl(a, stream);
+    return gemm_impl(a, nullptr, 0, stream);
+}
+
+extern "C" int tg_gemm_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                          tg_perm permA, const void* B, int64_t ldb, tg_perm permB, void* C,
+                          int64_t ldc, tg_dtype dtype, const tg_epilogue* epi, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+    Args a;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.A = A;
+    a.lda = lda;
+    a.permA = (int)permA;
+    a.B = B;
+    a.ldb = ldb;
+    a.permB = (int)permB;
+    a.C = C;
+    a.ldc = ldc;
+    a.dtype = (int)dtype;
+    a.bias = epi ? epi->bias_n : nullptr;
+    a.scale = epi ? epi->scale_m : nullptr;
+    a.resid = epi ? epi->residual : nullptr;
+    a.ldr = (epi && epi->residual) ? (epi->ldr ? epi->ldr : ldc) : 0;
+    a.relu = epi ? epi->relu : 0;
+    return gemm_impl(a, workspace, workspace_bytes, stream);
+}
+
+extern "C" int tg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, tg_dtype dtype,
+                                      tg_perm permA, tg_perm permB, const tg_epilogue* epi,
+                                      size_t* bytes) {
+    int rc = check_shape(M, N, K, (int)dtype, (int)permA, (int)permB, epi);
+    if (rc) return rc;
+    if (!bytes) return TG_ERR_INVALID_ARG;
+    int dev;
+    DeviceInfo* info;
+    if ((rc = current_device(&dev, &info))) return rc;
+    const bool has_epi = epi && (epi->bias_n || epi->scale_m || epi->residual || epi->relu);
+    const KernelConfig c = select_config(M, N, K, (int)dtype, (int)permA, (int)permB, has_epi,
+                                         info->sms, true);
+    *bytes = (size_t)c.ws_bytes;
+    return TG_OK;
 }
 
 extern "C" const char* tg_status_string(int status) {
@@ -364,8 +440,9 @@ extern "C" const char* tg_status_string(int status) {
     }
 }
 
-extern "C" int tg_query_config(int64_t M, int64_t N, int64_t K, tg_dtype dtype, tg_perm permA,
-                               tg_perm permB, const tg_epilogue* epi, char* buf, size_t len) {
+static int query_config(int stream_k, int64_t M, int64_t N, int64_t K, tg_dtype dtype,
+                        tg_perm permA, tg_perm permB, const tg_epilogue* epi, char* buf,
+                        size_t len) {
     int rc = check_shape(M, N, K, (int)dtype, (int)permA, (int)permB, epi);
     if (rc) return rc;
     if (!buf) return TG_ERR_INVALID_ARG;
@@ -374,21 +451,32 @@ extern "C" int tg_query_config(int64_t M, int64_t N, int64_t K, tg_dtype dtype, 
     if ((rc = current_device(&dev, &info))) return rc;
     const bool has_epi = epi && (epi->bias_n || epi->scale_m || epi->residual || epi->relu);
     const KernelConfig c = select_config(M, N, K, (int)dtype, (int)permA, (int)permB, has_epi,
-                                         info->sms);
+                                         info->sms, stream_k != 0);
     const std::string s = describe_config(c);
     if (s.size() + 1 > len) return TG_ERR_BUFFER;
     std::memcpy(buf, s.c_str(), s.size() + 1);
     return TG_OK;
 }
 
-extern "C" int tg_query_config_for_sms(int sms, int64_t M, int64_t N, int64_t K, tg_dtype dtype,
-                                       tg_perm permA, tg_perm permB, const tg_epilogue* epi,
-                                       char* buf, size_t len) {
+extern "C" int tg_query_config(int64_t M, int64_t N, int64_t K, tg_dtype dtype, tg_perm permA,
+                               tg_perm permB, const tg_epilogue* epi, char* buf, size_t len) {
+    return query_config(0, M, N, K, dtype, permA, permB, epi, buf, len);
+}
+
+extern "C" int tg_query_config_ws(int64_t M, int64_t N, int64_t K, tg_dtype dtype, tg_perm permA,
+                                  tg_perm permB, const tg_epilogue* epi, char* buf, size_t len) {
+    return query_config(1, M, N, K, dtype, permA, permB, epi, buf, len);
+}
+
+extern "C" int tg_query_config_for_sms(int sms, int stream_k, int64_t M, int64_t N, int64_t K,
+                                       tg_dtype dtype, tg_perm permA, tg_perm permB,
+                                       const tg_epilogue* epi, char* buf, size_t len) {
     int rc = check_shape(M, N, K, (int)dtype, (int)permA, (int)permB, epi);
     if (rc) return rc;
     if (!buf || sms < 2 || sms > 4096) return TG_ERR_INVALID_ARG;
     const bool has_epi = epi && (epi->bias_n || epi->scale_m || epi->residual || epi->relu);
-    const KernelConfig c = select_config(M, N, K, (int)dtype, (int)permA, (int)permB, has_epi, sms);
+    const KernelConfig c = select_config(M, N, K, (int)dtype, (int)permA, (int)permB, has_epi, sms,
+                                         stream_k != 0);
     const std::string s = describe_config(c);
     if (s.size() + 1 > len) return TG_ERR_BUFFER;
     std::memcpy(buf, s.c_str(), s.size() + 1);

@@ -2,7 +2,6 @@
 #include "gemm_launch.cuh"
 
 namespace tg {
-TG_INSTANTIATE(32, false, false)
-TG_INSTANTIATE(64, false, false)
-TG_INSTANTIATE(128, false, false)
+TG_INSTANTIATE(32, false, false, false)
+TG_INSTANTIATE(64, false, false, false)
 }  // namespace tg

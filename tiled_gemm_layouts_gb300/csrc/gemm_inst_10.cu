@@ -2,5 +2,5 @@
 #include "gemm_launch.cuh"
 
 namespace tg {
-TG_INSTANTIATE(224, true, true)
+TG_INSTANTIATE(192, false, false, true)
 }  // namespace tg

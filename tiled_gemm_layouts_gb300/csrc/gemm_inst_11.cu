@@ -2,5 +2,5 @@
 #include "gemm_launch.cuh"
 
 namespace tg {
-TG_INSTANTIATE(256, true, false)
+TG_INSTANTIATE(192, false, true, false)
 }  // namespace tg

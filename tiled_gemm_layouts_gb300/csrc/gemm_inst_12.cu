@@ -2,5 +2,5 @@
 #include "gemm_launch.cuh"
 
 namespace tg {
-TG_INSTANTIATE(256, true, true)
+TG_INSTANTIATE(192, false, true, true)
 }  // namespace tg

@@ -2,7 +2,6 @@
 #include "gemm_launch.cuh"
 
 namespace tg {
-TG_INSTANTIATE(32, false, true)
-TG_INSTANTIATE(64, false, true)
-TG_INSTANTIATE(128, false, true)
+TG_INSTANTIATE(32, false, false, true)
+TG_INSTANTIATE(64, false, false, true)
 }  // namespace tg

@@ -1,0 +1,6 @@
+// gemm_inst_23.cu -- explicit instantiations of some tile configurations.
+#include "gemm_launch.cuh"
+
+namespace tg {
+TG_INSTANTIATE(128, true, true, false)
+}  // namespace tg

@@ -2,6 +2,6 @@
 #include "gemm_launch.cuh"
 
 namespace tg {
-TG_INSTANTIATE(192, false, false)
-TG_INSTANTIATE(224, false, false)
+TG_INSTANTIATE(32, false, true, false)
+TG_INSTANTIATE(64, false, true, false)
 }  // namespace tg

@@ -2,6 +2,6 @@
 #include "gemm_launch.cuh"
 
 namespace tg {
-TG_INSTANTIATE(192, false, true)
-TG_INSTANTIATE(224, false, true)
+TG_INSTANTIATE(32, false, true, true)
+TG_INSTANTIATE(64, false, true, true)
 }  // namespace tg

@@ -2,5 +2,5 @@
 #include "gemm_launch.cuh"
 
 namespace tg {
-TG_INSTANTIATE(256, false, false)
+TG_INSTANTIATE(128, false, false, false)
 }  // namespace tg

@@ -2,5 +2,5 @@
 #include "gemm_launch.cuh"
 
 namespace tg {
-TG_INSTANTIATE(256, false, true)
+TG_INSTANTIATE(128, false, false, true)
 }  // namespace tg

@@ -2,6 +2,5 @@
 #include "gemm_launch.cuh"
 
 namespace tg {
-TG_INSTANTIATE(128, true, false)
-TG_INSTANTIATE(192, true, false)
+TG_INSTANTIATE(128, false, true, false)
 }  // namespace tg

@@ -2,6 +2,5 @@
 #include "gemm_launch.cuh"
 
 namespace tg {
-TG_INSTANTIATE(128, true, true)
-TG_INSTANTIATE(192, true, true)
+TG_INSTANTIATE(128, false, true, true)
 }  // namespace tg

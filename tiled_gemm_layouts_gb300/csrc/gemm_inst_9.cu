@@ -2,5 +2,5 @@
 #include "gemm_launch.cuh"
 
 namespace tg {
-TG_INSTANTIATE(224, true, false)
+TG_INSTANTIATE(192, false, false, false)
 }  // namespace tg

@@ -41,6 +41,7 @@ namespace tg {
 constexpr int kBK = 64;        // K elements per stage: one 128-byte swizzle row of fp16/bf16
 constexpr int kUmmaK = 16;     // K per tcgen05.mma of kind::f16
 constexpr int kThreads = 192;  // producer warp, MMA warp, four epilogue warps
+constexpr int kStageBufs = 4;  // output staging buffers per epilogue warp
 
 template <int BN, bool PAIR>
 struct TileShape {
@@ -50,10 +51,16 @@ struct TileShape {
     static constexpr int kAStage = 128 * kBK * 2;             // 16 KB
     static constexpr int kBStage = kBBoxes * 64 * kBK * 2;    // whole atoms
     static constexpr int kStage = kAStage + kBStage;
-    static constexpr int kStages = (200 * 1024 / kStage) > 8 ? 8 : (200 * 1024 / kStage);
+    // epilogue staging: per epilogue warp kStageBufs 32 x 32 output chunks (2 KB each)
+    static constexpr int kStaging = 4 * kStageBufs * 2048;
+    static constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block
+    static constexpr int kStagesFit = (kSmemLimit - 1024 - 256 - kStaging) / kStage;
+    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
     static constexpr int kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
                                    : 2 * BN <= 256 ? 256 : 512;
-    static constexpr int kSmemBytes = 1024 + kStages * kStage + (2 * kStages + 5) * 8 + 16;
+    static constexpr int kSmemBytes = 1024 + kStages * kStage + kStaging + (2 * kStages + 5) * 8 + 16;
+    static_assert(kStages >= 4, "too few pipeline stages");
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN: multiple of 32 in 32..256");
     static_assert(!PAIR || BN % 32 == 0, "pair tiles split BN in halves of 16-multiples");
 };
@@ -151,37 +158,62 @@ __device__ __forceinline__ bool prefetch_aux(const GemmParams& p, int m, int c0,
     return true;
 }
 
-// Epilogue of a full run C(m, c0 .. c0+31) with its operands already loaded.
-__device__ __forceinline__ void epilogue_run(const GemmParams& p, int m, int c0, float (&y)[32],
-                                             float row_scale, const Aux& a) {
+// Epilogue arithmetic for the run C(m, c0 .. c0+31) held in y[], in fp32:
+// scale, bias, ReLU, residual.  `a` holds the prefetched bias/residual of a
+// full in-bounds run; otherwise (edge runs) they are loaded here with
+// per-element masks.  Values outside C are computed but never stored.
+__device__ __forceinline__ void epilogue_math(const GemmParams& p, int m, int c0, float (&y)[32],
+                                              float row_scale, const Aux* a) {
     const int bf = p.bf16;
+    const bool inside = m < p.M && c0 < p.N;
+    const bool full = inside && c0 + 32 <= p.N;
     if (p.scale_m) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) y[j] *= row_scale;
     }
-    if (p.bias_n) {
+    if (p.bias_n && inside) {
+        const uint16_t* b = static_cast<const uint16_t*>(p.bias_n) + c0;
+        if (full) {
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            float f[8];
-            unpack8(a.b[v], f, bf);
+            for (int v = 0; v < 4; ++v) {
+                float f[8];
+                unpack8(a ? a->b[v] : __ldg(reinterpret_cast<const uint4*>(b) + v), f, bf);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) y[8 * v + i] += f[i];
+                for (int i = 0; i < 8; ++i) y[8 * v + i] += f[i];
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (c0 + j < p.N) y[j] += to_f32(b[j], bf);
         }
     }
     if (p.relu) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) y[j] = fmaxf(y[j], 0.0f);
     }
-    if (p.resid) {
+    if (p.resid && inside) {
+        const uint16_t* r = static_cast<const uint16_t*>(p.resid) + (long long)m * p.ldr + c0;
+        if (full) {
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            float f[8];
-            unpack8(a.r[v], f, bf);
+            for (int v = 0; v < 4; ++v) {
+                float f[8];
+                unpack8(a ? a->r[v] : __ldg(reinterpret_cast<const uint4*>(r) + v), f, bf);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) y[8 * v + i] += f[i];
+                for (int i = 0; i < 8; ++i) y[8 * v + i] += f[i];
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (c0 + j < p.N) y[j] += to_f32(r[j], bf);
         }
     }
-    uint4* c = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.C) + (long long)m * p.ldc + c0);
+}
+
+// Writes row `r` (0..31) of a 32 x 32 output chunk into its staging buffer:
+// 64-byte rows in the 64-byte XOR swizzle the C tensor map uses (16-byte
+// chunk index XOR (r / 2) mod 4), so the 32 lanes of a warp spread every
+// store over all banks.
+__device__ __forceinline__ void stage_row(uint8_t* buf, int r, const float (&y)[32], int bf) {
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
         uint4 u;
@@ -189,101 +221,121 @@ __device__ __forceinline__ void epilogue_run(const GemmParams& p, int m, int c0,
         u.y = pack2(y[8 * v + 2], y[8 * v + 3], bf);
         u.z = pack2(y[8 * v + 4], y[8 * v + 5], bf);
         u.w = pack2(y[8 * v + 6], y[8 * v + 7], bf);
-        c[v] = u;
+        *reinterpret_cast<uint4*>(buf + r * 64 + ((v ^ ((r >> 1) & 3)) << 4)) = u;
     }
 }
 
-// Epilogue for one 32-column chunk held by this thread: kernel row `rk`
-// (one TMEM lane), kernel columns c0 .. c0+31 in y[].  General path: edge
-// runs of C, and the swapped (transposed-output) layout.
-__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int rk, int c0,
-                                               float (&y)[32], float row_scale, float row_bias) {
-    const int bf = p.bf16;
-    if (!p.swap) {
-        // C(m = rk, n = c0 + j): a contiguous run of 32 outputs in one row.
-        const int m = rk;
-        if (m >= p.M || c0 >= p.N) return;
-        const bool full = c0 + 32 <= p.N;
-        if (p.scale_m) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) y[j] *= row_scale;
-        }
-        if (p.bias_n) {
-            const uint16_t* b = static_cast<const uint16_t*>(p.bias_n) + c0;
-            if (full) {
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    float f[8];
-                    unpack8(__ldg(reinterpret_cast<const uint4*>(b) + v), f, bf);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) y[8 * v + i] += f[i];
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (c0 + j < p.N) y[j] += to_f32(b[j], bf);
-            }
-        }
-        if (p.relu) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) y[j] = fmaxf(y[j], 0.0f);
-        }
-        if (p.resid) {
-            const uint16_t* r = static_cast<const uint16_t*>(p.resid) + (long long)m * p.ldr + c0;
-            if (full) {
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    float f[8];
-                    unpack8(__ldg(reinterpret_cast<const uint4*>(r) + v), f, bf);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) y[8 * v + i] += f[i];
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (c0 + j < p.N) y[j] += to_f32(r[j], bf);
-            }
-        }
-        uint16_t* c = static_cast<uint16_t*>(p.C) + (long long)m * p.ldc + c0;
-        if (full) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                uint4 u;
-                u.x = pack2(y[8 * v + 0], y[8 * v + 1], bf);
-                u.y = pack2(y[8 * v + 2], y[8 * v + 3], bf);
-                u.z = pack2(y[8 * v + 4], y[8 * v + 5], bf);
-                u.w = pack2(y[8 * v + 6], y[8 * v + 7], bf);
-                reinterpret_cast<uint4*>(c)[v] = u;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (c0 + j < p.N) c[j] = from_f32(y[j], bf);
-        }
-    } else {
-        // Swapped operands: kernel row rk is C's column n, kernel column c0+j is
-        // C's row m.  Lanes of a warp hold consecutive n, so every store
-        // instruction writes one contiguous run of a C row.
-        const int n = rk;
-        if (n >= p.N) return;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int m = c0 + j;
-            if (m >= p.M) continue;
-            float v = y[j];
-            if (p.scale_m) v *= to_f32(static_cast<const uint16_t*>(p.scale_m)[m], bf);
-            if (p.bias_n) v += row_bias;
-            if (p.relu) v = fmaxf(v, 0.0f);
-            if (p.resid) v += to_f32(static_cast<const uint16_t*>(p.resid)[(long long)m * p.ldr + n], bf);
-            static_cast<uint16_t*>(p.C)[(long long)m * p.ldc + n] = from_f32(v, bf);
-        }
+// One warp stores its 32 x 32 chunk C(row0.., c0..) through shared memory
+// with a TMA tensor store.  The tensor store clips rows at M and columns at
+// n_tma = N rounded down to 8 (it bounds the innermost dimension in whole
+// 16-byte units); the few columns [n_tma, N) of a row are stored directly.
+// kStageBufs staging buffers per warp rotate; `count` is the warp's running
+// chunk number.
+__device__ __forceinline__ void store_chunk(const GemmParams& p, uint8_t* stage, uint32_t& count,
+                                            int lane, int row0, int c0, const float (&y)[32]) {
+    uint8_t* buf = stage + (count % kStageBufs) * 2048;
+    if (count >= kStageBufs && lane == 0)
+        bulk_wait_group_read<kStageBufs - 1>();  // its previous store has read it
+    __syncwarp();
+    stage_row(buf, lane, y, p.bf16);
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+        if (row0 < p.M && c0 < p.n_tma) tma_store_2d(&p.map_c, smem_addr(buf), c0, row0);
+        bulk_commit_group();
     }
+    if (c0 + 32 > p.n_tma && c0 < p.N && row0 + lane < p.M) {
+        uint16_t* c = static_cast<uint16_t*>(p.C) + (long long)(row0 + lane) * p.ldc;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (c0 + j >= p.n_tma && c0 + j < p.N) c[c0 + j] = from_f32(y[j], p.bf16);
+    }
+    ++count;
+}
+
+// Epilogue of the swapped (transposed-output) layout for one 32-column chunk:
+// kernel row rk is C's column n, kernel column c0+j is C's row m.  Lanes of a
+// warp hold consecutive n, so every store instruction writes one contiguous
+// run of a C row.
+__device__ __forceinline__ void epilogue_swap(const GemmParams& p, int rk, int c0,
+                                              const float (&y)[32], float row_bias) {
+    const int bf = p.bf16;
+    const int n = rk;
+    if (n >= p.N) return;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int m = c0 + j;
+        if (m >= p.M) continue;
+        float v = y[j];
+        if (p.scale_m) v *= to_f32(static_cast<const uint16_t*>(p.scale_m)[m], bf);
+        if (p.bias_n) v += row_bias;
+        if (p.relu) v = fmaxf(v, 0.0f);
+        if (p.resid) v += to_f32(static_cast<const uint16_t*>(p.resid)[(long long)m * p.ldr + n], bf);
+        static_cast<uint16_t*>(p.C)[(long long)m * p.ldc + n] = from_f32(v, bf);
+    }
+}
+
+// The work items of one persistent worker: its whole tiles first (worker w
+// takes tiles w, w + workers, ... below dp_tiles), then its contiguous range
+// of stream-K iterations, cut at tile boundaries into (tile, k-block range).
+struct WorkIter {
+    int workers, dp_tiles, num_kb, dp_next;
+    long long it, it_end;
+
+    __device__ __forceinline__ WorkIter(const GemmParams& p, int worker)
+        : workers(p.workers), dp_tiles(p.dp_tiles), num_kb(p.num_kb), dp_next(worker),
+          it(p.sk_iters * worker / p.workers), it_end(p.sk_iters * (worker + 1) / p.workers) {}
+
+    __device__ __forceinline__ bool next(int& tile, int& kb0, int& kb1) {
+        if (dp_next < dp_tiles) {
+            tile = dp_next;
+            kb0 = 0;
+            kb1 = num_kb;
+            dp_next += workers;
+            return true;
+        }
+        if (it < it_end) {
+            const long long ts = it / num_kb;
+            tile = dp_tiles + (int)ts;
+            kb0 = (int)(it - ts * num_kb);
+            const long long left = it_end - it;
+            kb1 = (int)(left < (long long)(num_kb - kb0) ? kb0 + left : num_kb);
+            it += kb1 - kb0;
+            return true;
+        }
+        return false;
+    }
+};
+
+// Worker whose stream-K range holds iteration `it`.
+__device__ __forceinline__ int sk_owner(const GemmParams& p, long long it) {
+    int w = (int)(it * p.workers / p.sk_iters);
+    while (w + 1 < p.workers && p.sk_iters * (w + 1) / p.workers <= it) ++w;
+    while (w > 0 && p.sk_iters * w / p.workers > it) --w;
+    return w;
+}
+
+// Named barrier over the four epilogue warps that also ANDs a flag: every
+// epilogue thread leaves with the same decision.
+__device__ __forceinline__ int epilogue_sync_and(int v) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, 1, 128, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(out)
+        : "r"((uint32_t)v)
+        : "memory");
+    return (int)out;
 }
 
 // AUX = true: the epilogue reads a bias and/or residual; their loads are
 // issued one 32-column run ahead (and before the accumulator is ready).
 // AUX = false keeps the plain epilogue lean.
-template <int BN, bool PAIR, bool AUX>
+// SK = true: the launch deals tail tiles out in K-ranges (the stream-K code is
+// compiled only into these instantiations; whole-tile kernels stay lean).
+template <int BN, bool PAIR, bool AUX, bool SK>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
     using TS = TileShape<BN, PAIR>;
     constexpr int STAGES = TS::kStages;
@@ -294,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                                                ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * TS::kAStage;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * TS::kBStage);
+    uint8_t* staging = sB + STAGES * TS::kBStage;  // epilogue output chunks (1024-aligned)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + TS::kStaging);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
@@ -302,13 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* sk_last = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? cluster_ctarank() : 0;
     const bool leader = rank == 0;
-    const int cta_tile0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // first tile
-    const int tile_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const int worker = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const Watch w{abort_flag,
                   PAIR ? mapa_shared(smem_addr((const void*)abort_flag), rank ^ 1u) : 0u, PAIR,
                   p.status, p.timeout_cycles};
@@ -316,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (threadIdx.x == 0) {
         prefetch_tensormap(&p.map_p);
         prefetch_tensormap(&p.map_q);
+        prefetch_tensormap(&p.map_c);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
             mbar_init(smem_addr(&empty[s]), 1);
@@ -352,12 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const uint32_t a_bytes = TS::kAStage;
             const uint32_t b_bytes = p.q_mn_major ? (uint32_t)TS::kBStage : (uint32_t)TS::kBNC * 128u;
             const uint32_t stage_tx = (a_bytes + b_bytes) * (PAIR ? 2u : 1u);
-            for (int t = cta_tile0; ok && t < p.num_tiles; t += tile_step) {
+            WorkIter items(p, worker);
+            int t, kb0, kb1;
+            while (ok && items.next(t, kb0, kb1)) {
                 int tm, tn;
                 tile_coords(p, t, tm, tn);
                 const int m0 = tm * TS::kBM + (int)rank * 128;
                 const int n0 = tn * BN + (int)rank * TS::kBNC;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+                for (int kb = kb0; kb < kb1; ++kb, ++g) {
                     if (!wait_bar(smem_addr(&empty[stage]), phase ^ 1, w, DEV_TIMEOUT_PRODUCER)) {
                         ok = false;
                         break;
@@ -423,13 +479,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             uint32_t phase = 0;
             bool ok = true;
             int i = 0;
-            for (int t = cta_tile0; ok && t < p.num_tiles; t += tile_step, ++i) {
+            WorkIter items(p, worker);
+            int t, kb0, kb1;
+            for (; ok && items.next(t, kb0, kb1); ++i) {
                 const int buf = i & 1;
                 const uint32_t aph = (i >> 1) & 1;
                 if (!wait_bar(smem_addr(&tempty[buf]), aph ^ 1, w, DEV_TIMEOUT_MMA + 1)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bar(smem_addr(&full[stage]), phase, w, DEV_TIMEOUT_MMA + 2)) {
                         ok = false;
                         break;
@@ -447,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         const uint64_t bd = p.q_mn_major
                                                 ? smem_desc_sw128(b_addr + kk * 2048, 8192, 1024)
                                                 : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-                        mma_f16<CG>(d_tmem, ad, bd, p.idesc, (kb | kk) != 0);
+                        mma_f16<CG>(d_tmem, ad, bd, p.idesc, (kb != kb0) || (kk != 0));
                     }
                     // frees the stage (in both CTAs) once the MMAs have read it
                     if constexpr (PAIR)
@@ -476,20 +534,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     } else {
         // ---------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        uint8_t* stage = staging + (warp - 2) * kStageBufs * 2048;  // this warp's output buffers
+        uint32_t chunks = 0;                           // output chunks stored so far
         int i = 0;
-        for (int t = cta_tile0; t < p.num_tiles; t += tile_step, ++i) {
+        WorkIter items(p, worker);
+        int t, kb0, kb1;
+        for (; items.next(t, kb0, kb1); ++i) {
             const int buf = i & 1;
             const uint32_t aph = (i >> 1) & 1;
             int tm, tn;
             tile_coords(p, t, tm, tn);
             const int rk = tm * TS::kBM + (int)rank * 128 + q * 32 + lane;
+            const bool whole = !SK || (kb0 == 0 && kb1 == p.num_kb);
             // operands of the first run do not depend on the accumulator:
             // fetch them while the main loop still runs
             Aux cur, nxt;
-            bool cur_full = AUX ? prefetch_aux(p, rk, tn * BN, cur) : false;
+            bool cur_full = (AUX && whole) ? prefetch_aux(p, rk, tn * BN, cur) : false;
             int ok = 1;
             if (lane == 0) ok = wait_bar(smem_addr(&tfull[buf]), aph, w, DEV_TIMEOUT_EPILOGUE);
             ok = __shfl_sync(0xffffffffu, ok, 0);
+            ok = epilogue_sync_and(ok);  // all four warps continue, or all stop
             if (!ok) break;
             tc_fence_after();
             float row_scale = 1.0f, row_bias = 0.0f;
@@ -499,13 +563,141 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 if (p.bias_n && rk < p.N) row_bias = to_f32(static_cast<const uint16_t*>(p.bias_n)[rk], p.bf16);
             }
             const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
+            const int row0 = tm * TS::kBM + (int)rank * 128 + q * 32;  // this warp's first row
+            if (SK && !whole) {
+                // ---- stream-K part of tile t: publish this worker's partial sum
+                const long long f = (long long)(t - p.dp_tiles) * p.num_kb;
+                const int wf = sk_owner(p, f), wl = sk_owner(p, f + p.num_kb - 1);
+                const int contributors = wl - wf + 1, mine = worker - wf;
+                // slot k of this tile and CTA: 128 rows x BN fp32 stored as
+                // [BN/4][128 rows][4], so that the 32 lanes of a warp (32
+                // consecutive rows) move 512 contiguous bytes per access
+                const size_t slot = (size_t)TS::kBM * BN;
+                float* base = p.ws_partial + (size_t)wf * p.sk_cmax * slot +
+                              (size_t)rank * 128 * BN + (size_t)(q * 32 + lane) * 4;
+                int* counter = p.ws_count + wf * 2 + rank;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    __syncwarp();
+                    tmem_ld_32x32b_x32(t_row + c * 32, v);
+                    tmem_wait_ld();
+                    float4* dst = reinterpret_cast<float4*>(base + (size_t)mine * slot) + c * 8 * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        __stcg(dst + j * 128, make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
+                }
+                // all four warps' partial stores happen-before the release below
+                epilogue_sync_and(1);
+                if (warp == 2 && lane == 0) {
+                    const bool l = atomic_add_release_gpu(counter, 1) == contributors - 1;
+                    if (l) fence_acquire_gpu();  // the other partials are visible to this CTA
+                    *sk_last = l;
+                }
+                const bool last = epilogue_sync_and(1) && *sk_last;
+                if (!last) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (PAIR)
+                            mbar_arrive_cluster(smem_addr(&tempty[buf]), 0);
+                        else
+                            mbar_arrive(smem_addr(&tempty[buf]));
+                    }
+                    continue;
+                }
+                // last to arrive: every other partial is published; add them
+                // all in K order (own part from TMEM) and finish the tile.  The
+                // other contributor's next chunk is loaded while this one is
+                // finished (two contributors is the common case).
+                const int other = contributors == 2 ? 1 - mine : -1;
+                float4 pre[8];
+                if (other >= 0) {
+                    const float4* src = reinterpret_cast<const float4*>(base + (size_t)other * slot);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) pre[j] = __ldcg(src + j * 128);
+                }
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    __syncwarp();
+                    tmem_ld_32x32b_x32(t_row + c * 32, v);
+                    float4 cur4[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) cur4[j] = pre[j];
+                    if (other >= 0 && c + 1 < BN / 32) {
+                        const float4* src = reinterpret_cast<const float4*>(base + (size_t)other * slot) +
+                                            (c + 1) * 8 * 128;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) pre[j] = __ldcg(src + j * 128);
+                    }
+                    tmem_wait_ld();
+                    if (c == BN / 32 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if constexpr (PAIR)
+                                mbar_arrive_cluster(smem_addr(&tempty[buf]), 0);
+                            else
+                                mbar_arrive(smem_addr(&tempty[buf]));
+                        }
+                    }
+                    float y[32];
+                    if (other >= 0) {
+                        // two parts: p0 + p1 (fp32 addition of two terms is order-free)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            y[4 * j] = __uint_as_float(v[4 * j]) + cur4[j].x;
+                            y[4 * j + 1] = __uint_as_float(v[4 * j + 1]) + cur4[j].y;
+                            y[4 * j + 2] = __uint_as_float(v[4 * j + 2]) + cur4[j].z;
+                            y[4 * j + 3] = __uint_as_float(v[4 * j + 3]) + cur4[j].w;
+                        }
+                    } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) y[j] = 0.0f;
+                    for (int k = 0; k < contributors; ++k) {
+                        if (k == mine) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) y[j] += __uint_as_float(v[j]);
+                        } else {
+                            const float4* src =
+                                reinterpret_cast<const float4*>(base + (size_t)k * slot) + c * 8 * 128;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 u = __ldcg(src + j * 128);
+                                y[4 * j] += u.x;
+                                y[4 * j + 1] += u.y;
+                                y[4 * j + 2] += u.z;
+                                y[4 * j + 3] += u.w;
+                            }
+                        }
+                    }
+                    }
+                    if (p.swap) {
+                        epilogue_swap(p, rk, tn * BN + c * 32, y, row_bias);
+                    } else {
+                        epilogue_math(p, rk, tn * BN + c * 32, y, row_scale, nullptr);
+                        store_chunk(p, stage, chunks, lane, row0, tn * BN + c * 32, y);
+                    }
+                }
+                if (warp == 2 && lane == 0) *counter = 0;  // ready for the next call
+                continue;
+            }
+            // 64 accumulator columns per TMEM read (a 32-column read for the
+            // last odd chunk), then two 32-column chunks of epilogue
+            constexpr int kLoads = (BN + 63) / 64;
+#pragma unroll 1
+            for (int c2 = 0; c2 < kLoads; ++c2) {
+                uint32_t v[64];
+                const bool two = 2 * c2 + 1 < BN / 32;
                 __syncwarp();
-                tmem_ld_32x32b_x32(t_row + c * 32, v);
+                if (two)
+                    tmem_ld_32x32b_x64(t_row + c2 * 64, v);
+                else
+                    tmem_ld_32x32b_x32(t_row + c2 * 64, *reinterpret_cast<uint32_t(*)[32]>(v));
                 tmem_wait_ld();
-                if (c == BN / 32 - 1) {
+                if (c2 == kLoads - 1) {
                     // every column of this buffer is in registers: release it
                     tc_fence_before();
                     __syncwarp();
@@ -516,24 +708,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                             mbar_arrive(smem_addr(&tempty[buf]));
                     }
                 }
-                float y[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(v[j]);
-                if constexpr (AUX) {
-                    bool nxt_full = false;
-                    if (c + 1 < BN / 32)
-                        nxt_full = prefetch_aux(p, rk, tn * BN + (c + 1) * 32, nxt);
-                    if (cur_full)
-                        epilogue_run(p, rk, tn * BN + c * 32, y, row_scale, cur);
-                    else
-                        epilogue_chunk(p, rk, tn * BN + c * 32, y, row_scale, row_bias);
-                    cur = nxt;
-                    cur_full = nxt_full;
-                } else {
-                    epilogue_chunk(p, rk, tn * BN + c * 32, y, row_scale, row_bias);
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && !two) break;
+                    const int c = 2 * c2 + h;
+                    float y[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(v[32 * h + j]);
+                    if (p.swap) {
+                        epilogue_swap(p, rk, tn * BN + c * 32, y, row_bias);
+                        continue;
+                    }
+                    if constexpr (AUX) {
+                        bool nxt_full = false;
+                        if (c + 1 < BN / 32)
+                            nxt_full = prefetch_aux(p, rk, tn * BN + (c + 1) * 32, nxt);
+                        epilogue_math(p, rk, tn * BN + c * 32, y, row_scale, cur_full ? &cur : nullptr);
+                        cur = nxt;
+                        cur_full = nxt_full;
+                    } else {
+                        epilogue_math(p, rk, tn * BN + c * 32, y, row_scale, nullptr);
+                    }
+                    store_chunk(p, stage, chunks, lane, row0, tn * BN + c * 32, y);
                 }
             }
         }
+        if (lane == 0) bulk_wait_group<0>();  // every output chunk has reached global memory
     }
 
     tc_fence_before();

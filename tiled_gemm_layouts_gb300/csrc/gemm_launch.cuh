@@ -11,16 +11,16 @@
 
 namespace tg {
 
-template <int BN, bool PAIR, bool AUX>
+template <int BN, bool PAIR, bool AUX, bool SK>
 cudaError_t launch_config(const GemmParams& p, const KernelConfig& cfg, cudaStream_t stream);
 
 // Explicit instantiation of one configuration (in gemm_inst_*.cu).
-#define TG_INSTANTIATE(B, P, X)                                                           \
+#define TG_INSTANTIATE(B, P, X, S)                                                        \
     template <>                                                                           \
-    cudaError_t launch_config<B, P, X>(const GemmParams& p, const KernelConfig& cfg,       \
-                                       cudaStream_t stream) {                             \
+    cudaError_t launch_config<B, P, X, S>(const GemmParams& p, const KernelConfig& cfg,    \
+                                          cudaStream_t stream) {                          \
         using TS = TileShape<B, P>;                                                       \
-        auto kern = gemm_kernel<B, P, X>;                                                 \
+        auto kern = gemm_kernel<B, P, X, S>;                                              \
         cudaError_t e = cudaFuncSetAttribute(                                             \
             kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TS::kSmemBytes);           \
         if (e != cudaSuccess) return e;                                                   \

@@ -22,6 +22,7 @@ enum : int {
 struct alignas(128) GemmParams {
     CUtensorMap map_p;   // P operand: K-major box {64, BM} or MN-major box {64, 64}
     CUtensorMap map_q;   // Q operand: K-major box {64, BN} or MN-major box {64, 64}
+    CUtensorMap map_c;   // C for tensor stores: box {32 columns, 32 rows}, 64-byte swizzle
     int Mk, Nk, K;       // kernel-side problem (after the optional swap)
     int num_kb;          // ceil(K / 64)
     int tiles_m, tiles_n, num_tiles;
@@ -33,6 +34,7 @@ struct alignas(128) GemmParams {
     int bf16;            // element type of every operand: 0 fp16, 1 bf16
     // epilogue, in C's (m, n) coordinates
     int M, N;            // C is M x N
+    int n_tma;           // columns [0, n_tma) of C go through tensor stores (N rounded down to 8)
     void* C;
     long long ldc;
     const void* bias_n;  // [N] or null
@@ -40,6 +42,19 @@ struct alignas(128) GemmParams {
     const void* resid;   // [M, ldr] or null
     long long ldr;
     int relu;
+    // Work split over the persistent workers (clusters of a pair, or CTAs).
+    // Tiles [0, dp_tiles) in raster order are computed whole, worker w taking
+    // w, w + workers, ...  The remaining sk_tiles are cut into
+    // sk_tiles * num_kb K-block iterations dealt out in equal contiguous
+    // ranges ("stream-K"); a tile whose range is split is finished by the
+    // contributor that arrives last, summing the partials in K order.
+    int workers;
+    int dp_tiles;
+    int sk_tiles;
+    int sk_cmax;           // partial slots per split tile
+    long long sk_iters;    // sk_tiles * num_kb
+    float* ws_partial;     // [workers][sk_cmax][BM][BN] fp32 partial accumulators
+    int* ws_count;         // [workers][2] arrival counters, zero between calls
     // watchdog
     long long timeout_cycles;
     int* status;         // device status word
@@ -56,6 +71,9 @@ struct KernelConfig {
     int group_m;
     int grid;       // persistent CTAs
     int tiles;
+    int sk_tiles;   // tiles computed stream-K (0: every tile whole)
+    int sk_cmax;    // partial slots per split tile
+    long long ws_bytes;  // workspace the stream-K part needs
 };
 
 // Launches one persistent GEMM; returns a cudaError_t.

@@ -23,10 +23,13 @@ int gemm_stages(int bn, int pair) {
 cudaError_t launch_gemm(const GemmParams& p, const KernelConfig& cfg, int /*num_sms*/,
                         cudaStream_t stream) {
     const bool aux = p.bias_n != nullptr || p.resid != nullptr;
-#define TG_CASE(B, P)                                                            \
-    if (cfg.bn == B && cfg.pair == P)                                            \
-        return aux ? launch_config<B, P, true>(p, cfg, stream)                   \
-                   : launch_config<B, P, false>(p, cfg, stream);
+    const bool sk = p.sk_tiles > 0;
+#define TG_CASE(B, P)                                                                      \
+    if (cfg.bn == B && cfg.pair == P)                                                      \
+        return aux ? (sk ? launch_config<B, P, true, true>(p, cfg, stream)                 \
+                         : launch_config<B, P, true, false>(p, cfg, stream))               \
+                   : (sk ? launch_config<B, P, false, true>(p, cfg, stream)                \
+                         : launch_config<B, P, false, false>(p, cfg, stream));
     TG_FOR_EACH_CONFIG(TG_CASE)
 #undef TG_CASE
     return cudaErrorInvalidValue;

@@ -53,7 +53,8 @@ struct Choice {
     double score;
 };
 
-void apply_override(KernelConfig& c, bool& forced_bn, bool& forced_pair, bool& forced_swap) {
+void apply_override(KernelConfig& c, bool& forced_bn, bool& forced_pair, bool& forced_swap,
+                    bool& forced_no_sk) {
     const char* env = std::getenv("TG_FORCE_CONFIG");
     if (!env || !*env) return;
     char buf[256];
@@ -73,18 +74,30 @@ void apply_override(KernelConfig& c, bool& forced_bn, bool& forced_pair, bool& f
             c.group_m = v;
         } else if (std::sscanf(tok, "grid=%d", &v) == 1 && v >= 1) {
             c.grid = v;
+        } else if (std::sscanf(tok, "sk=%d", &v) == 1 && (v == 0 || v == 1)) {
+            forced_no_sk = v == 0;
         }
     }
 }
 
 }  // namespace
 
+// Waves a tile count costs on `slots` workers: whole waves when every tile is
+// computed by one worker; with stream-K the tiles of the last waves are
+// shared out in equal K-ranges, at a small price for the partial sums.
+double effective_waves(int64_t tiles, int slots, bool allow_sk) {
+    const double whole = (double)cdiv(tiles, slots);
+    if (!allow_sk) return whole;
+    const double sk = (double)tiles / slots + 0.1;
+    return sk < whole ? sk : whole;
+}
+
 KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int permA, int permB,
-                           bool /*has_epilogue*/, int sms) {
+                           bool /*has_epilogue*/, int sms, bool allow_sk) {
     KernelConfig c{};
     c.group_m = 8;
-    bool forced_bn = false, forced_pair = false, forced_swap = false;
-    apply_override(c, forced_bn, forced_pair, forced_swap);
+    bool forced_bn = false, forced_pair = false, forced_swap = false, forced_no_sk = false;
+    apply_override(c, forced_bn, forced_pair, forced_swap, forced_no_sk);
 
     Choice best{0, 0, 0, -1.0};
     for (int swap = 0; swap < 2; ++swap) {
@@ -102,9 +115,9 @@ KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int p
                 const int bm = pair ? 256 : 128;
                 const int slots = pair ? sms / 2 : sms;
                 const int64_t tiles = cdiv(Mk, bm) * cdiv(Nk, bn);
-                const int64_t waves = cdiv(tiles, slots);
+                const double waves = effective_waves(tiles, slots, allow_sk);
                 const int cols = staged_columns(bn, pair, q_mn);
-                double score = (double)Mk * (double)Nk / ((double)waves * slots * bm * cols) *
+                double score = (double)Mk * (double)Nk / (waves * slots * bm * cols) *
                                tile_efficiency(cols, pair);
                 // A one-tile-wide problem is bandwidth bound: the narrowest tile
                 // that covers it streams the other operand once per SM.
@@ -133,19 +146,45 @@ KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int p
     const int slots = c.pair ? sms / 2 : sms;
     int clusters = c.grid > 0 ? (c.pair ? c.grid / 2 : c.grid) : slots;
     if (clusters > slots) clusters = slots;
-    if (clusters > tiles) clusters = (int)tiles;
+    c.stages = gemm_stages(c.bn, c.pair);
+
+    // Stream-K for the tail: the last partial wave plus one whole wave are
+    // dealt out as equal K-ranges when that beats whole waves.
+    c.sk_tiles = 0;
+    c.sk_cmax = 0;
+    c.ws_bytes = 0;
+    const int64_t num_kb = cdiv(K, 64);
+    if (allow_sk && !forced_no_sk && tiles % clusters != 0 &&
+        (double)tiles / clusters + 0.1 < (double)cdiv(tiles, clusters)) {
+        const int64_t sk_tiles = tiles > clusters ? clusters + tiles % clusters : tiles;
+        const int64_t iters = sk_tiles * num_kb;
+        if (iters >= 2 * (int64_t)clusters) {
+            const int64_t per = iters / clusters;  // shortest range
+            int64_t cmax = (num_kb - 1) / per + 2;
+            if (cmax > clusters) cmax = clusters;
+            c.sk_tiles = (int)sk_tiles;
+            c.sk_cmax = (int)cmax;
+            c.ws_bytes = sk_workspace_bytes(clusters, (int)cmax, c.bm, c.bn);
+        }
+    }
+    if (c.sk_tiles == 0 && clusters > tiles) clusters = (int)tiles;
     if (clusters < 1) clusters = 1;
     c.grid = c.pair ? 2 * clusters : clusters;
-    c.stages = gemm_stages(c.bn, c.pair);
-    (void)K;
     return c;
+}
+
+long long sk_workspace_bytes(int workers, int cmax, int bm, int bn) {
+    const long long counters = ((long long)workers * 2 * 4 + 255) / 256 * 256;
+    return counters + (long long)workers * cmax * bm * bn * 4;
 }
 
 std::string describe_config(const KernelConfig& c) {
     char buf[256];
     std::snprintf(buf, sizeof(buf),
-                  "swap=%d bm=%d bn=%d pair=%d stages=%d group_m=%d grid=%d tiles=%d", c.swap,
-                  c.bm, c.bn, c.pair, c.stages, c.group_m, c.grid, c.tiles);
+                  "swap=%d bm=%d bn=%d pair=%d stages=%d group_m=%d grid=%d tiles=%d sk_tiles=%d "
+                  "sk_cmax=%d ws_bytes=%lld",
+                  c.swap, c.bm, c.bn, c.pair, c.stages, c.group_m, c.grid, c.tiles, c.sk_tiles,
+                  c.sk_cmax, c.ws_bytes);
     return buf;
 }
 
