@@ -81,9 +81,10 @@ def test_stream_k_split(tg):
     # whole waves: nothing to split
     c = cfg_sk(tg, 256 * 76 // 4, 1024, 4096, F16, 0, 0)  # 19 x 4 = 76 tiles
     assert c["sk_tiles"] == 0 and c["ws_bytes"] == 0
-    # fewer tiles than SMs: every tile is shared (up to 3 contributors)
-    c = cfg_sk(tg, 32, 16384, 16384, BF16, 0, 0)
-    assert (c["sk_tiles"], c["grid"], c["sk_cmax"]) == (128, 152, 3)
+    # fewer tiles than workers, full waves or shallow K: whole tiles only
+    assert cfg_sk(tg, 32, 16384, 16384, BF16, 0, 0)["sk_tiles"] == 0
+    assert cfg_sk(tg, 8192, 8192, 4096, F16, 0, 0)["sk_tiles"] == 0   # 13.5 waves: 96 % full
+    assert cfg_sk(tg, 4000, 3000, 1000, F16, 1, 0)["sk_tiles"] == 0   # 16 K-blocks
     # without a workspace the same shapes keep whole tiles
     assert cfg(tg, 4096, 4096, 4096, F16, 0, 0)["sk_tiles"] == 0
 
@@ -101,7 +102,7 @@ def test_stream_k_invariants(tg, seed):
     workers = c["grid"] // 2 if c["pair"] else c["grid"]
     kb = -(-K // 64)
     if c["sk_tiles"]:
-        assert c["sk_tiles"] <= c["tiles"]
+        assert c["sk_tiles"] <= c["tiles"] and c["tiles"] > workers and kb >= 32
         assert c["tiles"] % workers != 0
         assert c["sk_tiles"] * kb >= 2 * workers
         shortest = c["sk_tiles"] * kb // workers

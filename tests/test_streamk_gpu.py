@@ -45,14 +45,14 @@ def run_ws(tg, p, force, ldc=None, ws_extra=0, ws=None):
 
 CASES = [
     # (M, N, K, dtype, force, epilogue)
-    (640, 256, 640, F16, "pair=0,bn=128,grid=4", {}),
-    (700, 300, 1000, BF16, "pair=0,bn=128,grid=4", dict(bias=True, scale=True, residual=True, relu=True)),
-    (1000, 520, 1200, F16, "pair=1,bn=256,grid=10", {}),
-    (1000, 520, 1200, BF16, "pair=1,bn=256,grid=10", dict(bias=True, residual=True)),
-    (600, 700, 900, F16, "pair=1,bn=128,grid=8", dict(scale=True, relu=True)),
-    (520, 300, 2000, F16, "pair=0,bn=256,grid=8", {}),            # no whole-tile waves at all
-    (32, 1000, 2048, BF16, "pair=0,bn=32,swap=1,grid=16", dict(scale=True)),
-    (200, 900, 3000, F16, "pair=0,bn=64,grid=12", dict(bias=True)),
+    (640, 256, 640, F16, "pair=0,bn=128,grid=4,sk=1", {}),
+    (700, 300, 1000, BF16, "pair=0,bn=128,grid=4,sk=1", dict(bias=True, scale=True, residual=True, relu=True)),
+    (1000, 520, 1200, F16, "pair=1,bn=256,grid=10,sk=1", {}),
+    (1000, 520, 1200, BF16, "pair=1,bn=256,grid=10,sk=1", dict(bias=True, residual=True)),
+    (600, 700, 900, F16, "pair=1,bn=128,grid=8,sk=1", dict(scale=True, relu=True)),
+    (520, 300, 2000, F16, "pair=0,bn=256,grid=8,sk=1", {}),            # no whole-tile waves at all
+    (32, 1000, 2048, BF16, "pair=0,bn=32,swap=1,grid=16,sk=1", dict(scale=True)),
+    (200, 900, 3000, F16, "pair=0,bn=64,grid=12,sk=1", dict(bias=True)),
 ]
 
 
@@ -86,10 +86,10 @@ def test_stream_k_parity(tg, M, N, K, dtype, force, epi, perm):
 
 def test_stream_k_matches_whole_tiles_closely(tg):
     p = synthetic.gemm_problem(1000, 520, 1200, F16, 5)
-    c_sk, rc, cfg, _ = run_ws(tg, p, "pair=1,bn=256,grid=10")
+    c_sk, rc, cfg, _ = run_ws(tg, p, "pair=1,bn=256,grid=10,sk=1")
     assert rc == tg.TG_OK and cfg["sk_tiles"] > 0
     from helpers import run_gemm, decode
-    c_dp, rc = run_gemm(tg, p, force="pair=1,bn=256,grid=10")
+    c_dp, rc = run_gemm(tg, p, force="pair=1,bn=256,grid=10,sk=1")
     assert rc == tg.TG_OK
     a, b = decode(c_sk, F16), decode(c_dp, F16)
     # both round the same fp32 sum computed in a different association
@@ -102,7 +102,7 @@ def test_workspace_checks(tg):
     A, B = dev(p["A"]), dev(p["B"])
     C = torch.empty((640, 256), dtype=torch.int16, device="cuda")
     old = os.environ.get("TG_FORCE_CONFIG")
-    os.environ["TG_FORCE_CONFIG"] = "pair=0,bn=128,grid=4"
+    os.environ["TG_FORCE_CONFIG"] = "pair=0,bn=128,grid=4,sk=1"
     try:
         need = tg.tg_gemm_workspace_size(640, 256, 640, F16)
         assert need > 0

@@ -40,7 +40,8 @@ namespace tg {
 
 constexpr int kBK = 64;        // K elements per stage: one 128-byte swizzle row of fp16/bf16
 constexpr int kUmmaK = 16;     // K per tcgen05.mma of kind::f16
-constexpr int kThreads = 192;  // producer warp, MMA warp, four epilogue warps
+constexpr int kEpiWarps = 4;   // one epilogue warp per TMEM lane quadrant (8 measured 7 % slower)
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, epilogue warps
 constexpr int kStageBufs = 4;  // output staging buffers per epilogue warp
 
 template <int BN, bool PAIR>
@@ -52,7 +53,7 @@ struct TileShape {
     static constexpr int kBStage = kBBoxes * 64 * kBK * 2;    // whole atoms
     static constexpr int kStage = kAStage + kBStage;
     // epilogue staging: per epilogue warp kStageBufs 32 x 32 output chunks (2 KB each)
-    static constexpr int kStaging = 4 * kStageBufs * 2048;
+    static constexpr int kStaging = kEpiWarps * kStageBufs * 2048;
     static constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block
     static constexpr int kStagesFit = (kSmemLimit - 1024 - 256 - kStaging) / kStage;
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
@@ -322,10 +323,10 @@ __device__ __forceinline__ int epilogue_sync_and(int v) {
     asm volatile(
         "{\n\t.reg .pred pi, po;\n\t"
         "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.and.pred po, 1, 128, pi;\n\t"
+        "bar.red.and.pred po, 1, %2, pi;\n\t"
         "selp.u32 %0, 1, 0, po;\n\t}"
         : "=r"(out)
-        : "r"((uint32_t)v)
+        : "r"((uint32_t)v), "n"(32 * kEpiWarps)
         : "memory");
     return (int)out;
 }
@@ -376,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&tfull[b]), 1);
-            mbar_init(smem_addr(&tempty[b]), PAIR ? 8 : 4);  // one arrival per epilogue warp
+            mbar_init(smem_addr(&tempty[b]), (PAIR ? 2 : 1) * kEpiWarps);  // one per epilogue warp
         }
         mbar_init(smem_addr(drain), 1);
         *abort_flag = 0;
@@ -534,6 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     } else {
         // ---------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        // the two warps of a quadrant split the tile's 32-column chunks
+        constexpr int kChunks = BN / 32;
+        const int half = (warp - 2) / 4;
+        const int c_begin = half ? (kChunks + 1) / 2 : 0;
+        const int c_end = half ? kChunks : (kChunks + 1) / 2;
         uint8_t* stage = staging + (warp - 2) * kStageBufs * 2048;  // this warp's output buffers
         uint32_t chunks = 0;                           // output chunks stored so far
         int i = 0;
@@ -549,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             // operands of the first run do not depend on the accumulator:
             // fetch them while the main loop still runs
             Aux cur, nxt;
-            bool cur_full = (AUX && whole) ? prefetch_aux(p, rk, tn * BN, cur) : false;
+            bool cur_full = (AUX && whole) ? prefetch_aux(p, rk, tn * BN + c_begin * 32, cur) : false;
             int ok = 1;
             if (lane == 0) ok = wait_bar(smem_addr(&tfull[buf]), aph, w, DEV_TIMEOUT_EPILOGUE);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -564,6 +570,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
             const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
             const int row0 = tm * TS::kBM + (int)rank * 128 + q * 32;  // this warp's first row
+            if (c_begin == c_end) {
+                // no columns for this warp (narrow tile): release the buffer at once
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (PAIR)
+                        mbar_arrive_cluster(smem_addr(&tempty[buf]), 0);
+                    else
+                        mbar_arrive(smem_addr(&tempty[buf]));
+                }
+            }
             if (SK && !whole) {
                 // ---- stream-K part of tile t: publish this worker's partial sum
                 const long long f = (long long)(t - p.dp_tiles) * p.num_kb;
@@ -576,8 +593,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 float* base = p.ws_partial + (size_t)wf * p.sk_cmax * slot +
                               (size_t)rank * 128 * BN + (size_t)(q * 32 + lane) * 4;
                 int* counter = p.ws_count + wf * 2 + rank;
+                // If every other part is already published this worker finishes
+                // the tile at once and never writes its own partial.
+                if (warp == 2 && lane == 0) {
+                    int seen;
+                    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(seen) : "l"(counter) : "memory");
+                    *sk_last = seen == contributors - 1;
+                }
+                const bool early_last = epilogue_sync_and(1) && *sk_last;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = c_begin; c < c_end && !early_last; ++c) {
                     uint32_t v[32];
                     __syncwarp();
                     tmem_ld_32x32b_x32(t_row + c * 32, v);
@@ -588,18 +613,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         __stcg(dst + j * 128, make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
                                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
                 }
-                // all four warps' partial stores happen-before the release below
-                epilogue_sync_and(1);
-                if (warp == 2 && lane == 0) {
-                    const bool l = atomic_add_release_gpu(counter, 1) == contributors - 1;
-                    if (l) fence_acquire_gpu();  // the other partials are visible to this CTA
-                    *sk_last = l;
+                bool last = early_last;
+                if (!early_last) {
+                    // all four warps' partial stores happen-before the release below
+                    epilogue_sync_and(1);
+                    if (warp == 2 && lane == 0) {
+                        const bool l = atomic_add_release_gpu(counter, 1) == contributors - 1;
+                        if (l) fence_acquire_gpu();  // the other partials are visible to this CTA
+                        *sk_last = l;
+                    }
+                    last = epilogue_sync_and(1) && *sk_last;
                 }
-                const bool last = epilogue_sync_and(1) && *sk_last;
                 if (!last) {
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) {
+                    if (lane == 0 && c_begin != c_end) {
                         if constexpr (PAIR)
                             mbar_arrive_cluster(smem_addr(&tempty[buf]), 0);
                         else
@@ -614,26 +642,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const int other = contributors == 2 ? 1 - mine : -1;
                 float4 pre[8];
                 if (other >= 0) {
-                    const float4* src = reinterpret_cast<const float4*>(base + (size_t)other * slot);
+                    const float4* src = reinterpret_cast<const float4*>(base + (size_t)other * slot) +
+                                        c_begin * 8 * 128;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) pre[j] = __ldcg(src + j * 128);
                 }
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = c_begin; c < c_end; ++c) {
                     uint32_t v[32];
                     __syncwarp();
                     tmem_ld_32x32b_x32(t_row + c * 32, v);
                     float4 cur4[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) cur4[j] = pre[j];
-                    if (other >= 0 && c + 1 < BN / 32) {
+                    if (other >= 0 && c + 1 < c_end) {
                         const float4* src = reinterpret_cast<const float4*>(base + (size_t)other * slot) +
                                             (c + 1) * 8 * 128;
 #pragma unroll
                         for (int j = 0; j < 8; ++j) pre[j] = __ldcg(src + j * 128);
                     }
                     tmem_wait_ld();
-                    if (c == BN / 32 - 1) {
+                    if (c == c_end - 1) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) {
@@ -684,20 +713,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 if (warp == 2 && lane == 0) *counter = 0;  // ready for the next call
                 continue;
             }
-            // 64 accumulator columns per TMEM read (a 32-column read for the
-            // last odd chunk), then two 32-column chunks of epilogue
-            constexpr int kLoads = (BN + 63) / 64;
 #pragma unroll 1
-            for (int c2 = 0; c2 < kLoads; ++c2) {
-                uint32_t v[64];
-                const bool two = 2 * c2 + 1 < BN / 32;
+            for (int c = c_begin; c < c_end; ++c) {
+                uint32_t v[32];
                 __syncwarp();
-                if (two)
-                    tmem_ld_32x32b_x64(t_row + c2 * 64, v);
-                else
-                    tmem_ld_32x32b_x32(t_row + c2 * 64, *reinterpret_cast<uint32_t(*)[32]>(v));
+                tmem_ld_32x32b_x32(t_row + c * 32, v);
                 tmem_wait_ld();
-                if (c2 == kLoads - 1) {
+                if (c == c_end - 1) {
                     // every column of this buffer is in registers: release it
                     tc_fence_before();
                     __syncwarp();
@@ -708,29 +730,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                             mbar_arrive(smem_addr(&tempty[buf]));
                     }
                 }
+                float y[32];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (h == 1 && !two) break;
-                    const int c = 2 * c2 + h;
-                    float y[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(v[32 * h + j]);
-                    if (p.swap) {
-                        epilogue_swap(p, rk, tn * BN + c * 32, y, row_bias);
-                        continue;
-                    }
-                    if constexpr (AUX) {
-                        bool nxt_full = false;
-                        if (c + 1 < BN / 32)
-                            nxt_full = prefetch_aux(p, rk, tn * BN + (c + 1) * 32, nxt);
-                        epilogue_math(p, rk, tn * BN + c * 32, y, row_scale, cur_full ? &cur : nullptr);
-                        cur = nxt;
-                        cur_full = nxt_full;
-                    } else {
-                        epilogue_math(p, rk, tn * BN + c * 32, y, row_scale, nullptr);
-                    }
-                    store_chunk(p, stage, chunks, lane, row0, tn * BN + c * 32, y);
+                for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(v[j]);
+                if (p.swap) {
+                    epilogue_swap(p, rk, tn * BN + c * 32, y, row_bias);
+                    continue;
                 }
+                if constexpr (AUX) {
+                    bool nxt_full = false;
+                    if (c + 1 < c_end)
+                        nxt_full = prefetch_aux(p, rk, tn * BN + (c + 1) * 32, nxt);
+                    epilogue_math(p, rk, tn * BN + c * 32, y, row_scale, cur_full ? &cur : nullptr);
+                    cur = nxt;
+                    cur_full = nxt_full;
+                } else {
+                    epilogue_math(p, rk, tn * BN + c * 32, y, row_scale, nullptr);
+                }
+                store_chunk(p, stage, chunks, lane, row0, tn * BN + c * 32, y);
             }
         }
         if (lane == 0) bulk_wait_group<0>();  // every output chunk has reached global memory

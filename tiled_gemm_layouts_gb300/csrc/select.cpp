@@ -54,7 +54,7 @@ struct Choice {
 };
 
 void apply_override(KernelConfig& c, bool& forced_bn, bool& forced_pair, bool& forced_swap,
-                    bool& forced_no_sk) {
+                    bool& forced_no_sk, bool& forced_sk) {
     const char* env = std::getenv("TG_FORCE_CONFIG");
     if (!env || !*env) return;
     char buf[256];
@@ -76,6 +76,7 @@ void apply_override(KernelConfig& c, bool& forced_bn, bool& forced_pair, bool& f
             c.grid = v;
         } else if (std::sscanf(tok, "sk=%d", &v) == 1 && (v == 0 || v == 1)) {
             forced_no_sk = v == 0;
+            forced_sk = v == 1;
         }
     }
 }
@@ -88,16 +89,18 @@ void apply_override(KernelConfig& c, bool& forced_bn, bool& forced_pair, bool& f
 double effective_waves(int64_t tiles, int slots, bool allow_sk) {
     const double whole = (double)cdiv(tiles, slots);
     if (!allow_sk) return whole;
-    const double sk = (double)tiles / slots + 0.1;
-    return sk < whole ? sk : whole;
+    const double fill = (double)tiles / (whole * slots);
+    if (tiles <= slots || fill >= 0.9) return whole;
+    return (double)tiles / slots + 0.25;
 }
 
 KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int permA, int permB,
                            bool /*has_epilogue*/, int sms, bool allow_sk) {
     KernelConfig c{};
     c.group_m = 8;
-    bool forced_bn = false, forced_pair = false, forced_swap = false, forced_no_sk = false;
-    apply_override(c, forced_bn, forced_pair, forced_swap, forced_no_sk);
+    bool forced_bn = false, forced_pair = false, forced_swap = false, forced_no_sk = false,
+         forced_sk = false;
+    apply_override(c, forced_bn, forced_pair, forced_swap, forced_no_sk, forced_sk);
 
     Choice best{0, 0, 0, -1.0};
     for (int swap = 0; swap < 2; ++swap) {
@@ -154,8 +157,13 @@ KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int p
     c.sk_cmax = 0;
     c.ws_bytes = 0;
     const int64_t num_kb = cdiv(K, 64);
-    if (allow_sk && !forced_no_sk && tiles % clusters != 0 &&
-        (double)tiles / clusters + 0.1 < (double)cdiv(tiles, clusters)) {
+    // Measured on GB300: the split pays when whole waves leave at least 10 %
+    // of the SM-time idle, every worker also has whole tiles, and tiles are
+    // at least 32 K-blocks deep (the partial sums cost about half a tile).
+    const double wave_fill = (double)tiles / ((double)cdiv(tiles, clusters) * clusters);
+    const bool want_sk = forced_sk ? tiles % clusters != 0
+                                   : (tiles > clusters && wave_fill < 0.9 && num_kb >= 32);
+    if (allow_sk && !forced_no_sk && want_sk) {
         const int64_t sk_tiles = tiles > clusters ? clusters + tiles % clusters : tiles;
         const int64_t iters = sk_tiles * num_kb;
         if (iters >= 2 * (int64_t)clusters) {
