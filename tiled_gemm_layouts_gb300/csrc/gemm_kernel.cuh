@@ -535,11 +535,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     } else {
         // ---------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
-        // the two warps of a quadrant split the tile's 32-column chunks
+        // the warps of a quadrant (kEpiWarps / 4 of them) split the tile's
+        // 32-column chunks
         constexpr int kChunks = BN / 32;
-        const int half = (warp - 2) / 4;
-        const int c_begin = half ? (kChunks + 1) / 2 : 0;
-        const int c_end = half ? kChunks : (kChunks + 1) / 2;
+        constexpr int kPerQuadrant = kEpiWarps / 4;
+        const int part = (warp - 2) / 4;
+        const int c_begin = part * kChunks / kPerQuadrant;
+        const int c_end = (part + 1) * kChunks / kPerQuadrant;
         uint8_t* stage = staging + (warp - 2) * kStageBufs * 2048;  // this warp's output buffers
         uint32_t chunks = 0;                           // output chunks stored so far
         int i = 0;
