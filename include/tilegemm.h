@@ -122,6 +122,34 @@ int tg_gemm_ws(int64_t M, int64_t N, int64_t K,
                const tg_epilogue* epi, void* workspace, size_t workspace_bytes,
                cudaStream_t stream);
 
+/*
+ * tg_gemm_ws without a caller workspace, for callers that cannot allocate
+ * device memory: code running inside a CUDA stream capture (a cudaMalloc
+ * there breaks the capture), code whose device memory is owned by an outside
+ * allocator, or plugins whose host framework forbids allocations.  The pages
+ * this library follows have no counterpart of this call; it exists for these
+ * callers only.
+ *
+ * The stream-K scratch is one statically allocated device array of 40 MiB
+ * (41943040 bytes) that every GPU loading this library keeps until the
+ * process exits; nothing is allocated per call (no cudaMalloc, no cudaFree,
+ * no allocating library routine).  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress): make that first call before
+ * any stream capture on that device.  Each call zeroes the array's counters
+ * on `stream` (cudaMemsetAsync) before its kernel.  Every call shares the
+ * one array: calls whose kernels overlap on the GPU (other streams, other
+ * host threads) race and corrupt each other's results -- serialise them.
+ *
+ * Arguments, checks and errors as tg_gemm_ws; TG_ERR_BUFFER when the split
+ * would need more scratch than the array holds (tg_gemm_workspace_size()
+ * above 41943040).  Shapes that need no split run whole tiles.
+ */
+int tg_gemm_static_ws(int64_t M, int64_t N, int64_t K,
+                      const void* A, int64_t lda, tg_perm permA,
+                      const void* B, int64_t ldb, tg_perm permB,
+                      void* C, int64_t ldc, tg_dtype dtype,
+                      const tg_epilogue* epi, cudaStream_t stream);
+
 /* Workspace bytes tg_gemm_ws needs for these arguments on the current device
  * (0 when every tile is computed whole). */
 int tg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, tg_dtype dtype, tg_perm permA,
