@@ -179,6 +179,15 @@ def workload_specs():
         "fp16_8192x8192x4096_fused": dict(M=8192, N=8192, K=4096, dtype=S.F16, seed=1003,
                                           bias=True, scale=True, residual=True, relu=True),
         "fp16_8192x8192x4096_plain": dict(M=8192, N=8192, K=4096, dtype=S.F16, seed=1003),
+        # profiling cases of the fused / plain kernels (inputs exceed L2, ~0.5 GB on the device)
+        "fp16_6144x6144x4096_fused": dict(M=6144, N=6144, K=4096, dtype=S.F16, seed=1003,
+                                          bias=True, scale=True, residual=True, relu=True),
+        "fp16_6144x6144x4096_plain": dict(M=6144, N=6144, K=4096, dtype=S.F16, seed=1003),
+        # the fused epilogue's parts, for attributing its cost
+        "fp16_8192x8192x4096_scale_bias_relu": dict(M=8192, N=8192, K=4096, dtype=S.F16,
+                                                    seed=1003, bias=True, scale=True, relu=True),
+        "fp16_8192x8192x4096_residual": dict(M=8192, N=8192, K=4096, dtype=S.F16, seed=1003,
+                                             residual=True),
         "fp16_4000x3000x1000_strided": dict(M=4000, N=3000, K=1000, dtype=S.F16, seed=1004,
                                             permA=1, ldb=3064, dist="normal", bias=True),
         "bf16_16384x1024x8192_scale": dict(M=16384, N=1024, K=8192, dtype=S.BF16, seed=1005,

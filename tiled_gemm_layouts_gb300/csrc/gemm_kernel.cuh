@@ -121,16 +121,40 @@ __device__ __forceinline__ uint16_t from_f32(float x, int bf16) {
     return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
 }
 
-__device__ __forceinline__ uint32_t pack2(float a, float b, int bf16) {
-    return (uint32_t)from_f32(a, bf16) | ((uint32_t)from_f32(b, bf16) << 16);
+// Two 16-bit values packed in a word -> two floats / two floats -> one word
+// with round-to-nearest-even, for a dtype fixed at compile time.
+template <bool BF>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    if constexpr (BF) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    } else {
+        __half2 h;
+        *reinterpret_cast<uint32_t*>(&h) = w;
+        return __half22float2(h);
+    }
 }
 
-__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8], int bf16) {
+template <bool BF>
+__device__ __forceinline__ uint32_t pack2t(float a, float b) {
+    uint32_t w;
+    if constexpr (BF) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        w = *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(a, b);
+        w = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return w;
+}
+
+template <bool BF>
+__device__ __forceinline__ void add8(const uint4& u, float* y) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        f[2 * i] = to_f32((uint16_t)(w[i] & 0xFFFFu), bf16);
-        f[2 * i + 1] = to_f32((uint16_t)(w[i] >> 16), bf16);
+        const float2 f = unpack2<BF>(w[i]);
+        y[2 * i] += f.x;
+        y[2 * i + 1] += f.y;
     }
 }
 
@@ -163,9 +187,9 @@ __device__ __forceinline__ bool prefetch_aux(const GemmParams& p, int m, int c0,
 // scale, bias, ReLU, residual.  `a` holds the prefetched bias/residual of a
 // full in-bounds run; otherwise (edge runs) they are loaded here with
 // per-element masks.  Values outside C are computed but never stored.
+template <bool BF>
 __device__ __forceinline__ void epilogue_math(const GemmParams& p, int m, int c0, float (&y)[32],
                                               float row_scale, const Aux* a) {
-    const int bf = p.bf16;
     const bool inside = m < p.M && c0 < p.N;
     const bool full = inside && c0 + 32 <= p.N;
     if (p.scale_m) {
@@ -176,16 +200,12 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int m, int c0
         const uint16_t* b = static_cast<const uint16_t*>(p.bias_n) + c0;
         if (full) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                float f[8];
-                unpack8(a ? a->b[v] : __ldg(reinterpret_cast<const uint4*>(b) + v), f, bf);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) y[8 * v + i] += f[i];
-            }
+            for (int v = 0; v < 4; ++v)
+                add8<BF>(a ? a->b[v] : __ldg(reinterpret_cast<const uint4*>(b) + v), y + 8 * v);
         } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (c0 + j < p.N) y[j] += to_f32(b[j], bf);
+                if (c0 + j < p.N) y[j] += to_f32(b[j], BF);
         }
     }
     if (p.relu) {
@@ -196,16 +216,12 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int m, int c0
         const uint16_t* r = static_cast<const uint16_t*>(p.resid) + (long long)m * p.ldr + c0;
         if (full) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                float f[8];
-                unpack8(a ? a->r[v] : __ldg(reinterpret_cast<const uint4*>(r) + v), f, bf);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) y[8 * v + i] += f[i];
-            }
+            for (int v = 0; v < 4; ++v)
+                add8<BF>(a ? a->r[v] : __ldg(reinterpret_cast<const uint4*>(r) + v), y + 8 * v);
         } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (c0 + j < p.N) y[j] += to_f32(r[j], bf);
+                if (c0 + j < p.N) y[j] += to_f32(r[j], BF);
         }
     }
 }
@@ -214,14 +230,15 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int m, int c0
 // 64-byte rows in the 64-byte XOR swizzle the C tensor map uses (16-byte
 // chunk index XOR (r / 2) mod 4), so the 32 lanes of a warp spread every
 // store over all banks.
-__device__ __forceinline__ void stage_row(uint8_t* buf, int r, const float (&y)[32], int bf) {
+template <bool BF>
+__device__ __forceinline__ void stage_row(uint8_t* buf, int r, const float (&y)[32]) {
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
         uint4 u;
-        u.x = pack2(y[8 * v + 0], y[8 * v + 1], bf);
-        u.y = pack2(y[8 * v + 2], y[8 * v + 3], bf);
-        u.z = pack2(y[8 * v + 4], y[8 * v + 5], bf);
-        u.w = pack2(y[8 * v + 6], y[8 * v + 7], bf);
+        u.x = pack2t<BF>(y[8 * v + 0], y[8 * v + 1]);
+        u.y = pack2t<BF>(y[8 * v + 2], y[8 * v + 3]);
+        u.z = pack2t<BF>(y[8 * v + 4], y[8 * v + 5]);
+        u.w = pack2t<BF>(y[8 * v + 6], y[8 * v + 7]);
         *reinterpret_cast<uint4*>(buf + r * 64 + ((v ^ ((r >> 1) & 3)) << 4)) = u;
     }
 }
@@ -232,13 +249,14 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int r, const float (&y)[
 // 16-byte units); the few columns [n_tma, N) of a row are stored directly.
 // kStageBufs staging buffers per warp rotate; `count` is the warp's running
 // chunk number.
+template <bool BF>
 __device__ __forceinline__ void store_chunk(const GemmParams& p, uint8_t* stage, uint32_t& count,
                                             int lane, int row0, int c0, const float (&y)[32]) {
     uint8_t* buf = stage + (count % kStageBufs) * 2048;
     if (count >= kStageBufs && lane == 0)
         bulk_wait_group_read<kStageBufs - 1>();  // its previous store has read it
     __syncwarp();
-    stage_row(buf, lane, y, p.bf16);
+    stage_row<BF>(buf, lane, y);
     fence_proxy_async_shared();
     __syncwarp();
     if (lane == 0) {
@@ -249,9 +267,23 @@ __device__ __forceinline__ void store_chunk(const GemmParams& p, uint8_t* stage,
         uint16_t* c = static_cast<uint16_t*>(p.C) + (long long)(row0 + lane) * p.ldc;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            if (c0 + j >= p.n_tma && c0 + j < p.N) c[c0 + j] = from_f32(y[j], p.bf16);
+            if (c0 + j >= p.n_tma && c0 + j < p.N) c[c0 + j] = from_f32(y[j], BF);
     }
     ++count;
+}
+
+// Epilogue arithmetic and store of one 32-column chunk, with the element type
+// resolved once per chunk (instead of per element).
+__device__ __forceinline__ void finish_chunk(const GemmParams& p, uint8_t* stage, uint32_t& count,
+                                             int lane, int rk, int row0, int c0, float (&y)[32],
+                                             float row_scale, const Aux* a) {
+    if (p.bf16) {
+        epilogue_math<true>(p, rk, c0, y, row_scale, a);
+        store_chunk<true>(p, stage, count, lane, row0, c0, y);
+    } else {
+        epilogue_math<false>(p, rk, c0, y, row_scale, a);
+        store_chunk<false>(p, stage, count, lane, row0, c0, y);
+    }
 }
 
 // Epilogue of the swapped (transposed-output) layout for one 32-column chunk:
@@ -708,8 +740,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     if (p.swap) {
                         epilogue_swap(p, rk, tn * BN + c * 32, y, row_bias);
                     } else {
-                        epilogue_math(p, rk, tn * BN + c * 32, y, row_scale, nullptr);
-                        store_chunk(p, stage, chunks, lane, row0, tn * BN + c * 32, y);
+                        finish_chunk(p, stage, chunks, lane, rk, row0, tn * BN + c * 32, y, row_scale,
+                                     nullptr);
                     }
                 }
                 if (warp == 2 && lane == 0) *counter = 0;  // ready for the next call
@@ -743,13 +775,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     bool nxt_full = false;
                     if (c + 1 < c_end)
                         nxt_full = prefetch_aux(p, rk, tn * BN + (c + 1) * 32, nxt);
-                    epilogue_math(p, rk, tn * BN + c * 32, y, row_scale, cur_full ? &cur : nullptr);
+                    finish_chunk(p, stage, chunks, lane, rk, row0, tn * BN + c * 32, y, row_scale,
+                                 cur_full ? &cur : nullptr);
                     cur = nxt;
                     cur_full = nxt_full;
                 } else {
-                    epilogue_math(p, rk, tn * BN + c * 32, y, row_scale, nullptr);
+                    finish_chunk(p, stage, chunks, lane, rk, row0, tn * BN + c * 32, y, row_scale,
+                                 nullptr);
                 }
-                store_chunk(p, stage, chunks, lane, row0, tn * BN + c * 32, y);
             }
         }
         if (lane == 0) bulk_wait_group<0>();  // every output chunk has reached global memory
