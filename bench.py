@@ -2,7 +2,10 @@
 
 Headline: fp16 GEMM C = A.B, M = N = K = 4096, row-major, entries uniform[-1,1]
 from seed 1002, fp32 accumulation, fp16 output; TFLOP/s = 2 M N K / kernel
-time.  One step = one tg_gemm call.  The 96 MB working set is smaller than
+time.  One step = one tg_gemm_ws call: whole output tiles plus, where the
+tile count leaves the last wave part-empty, the tail tiles shared out in
+K-ranges through a caller workspace (tg_gemm, without a workspace, runs whole
+tiles only; --no-stream-k times that).  The 96 MB working set is smaller than
 L2, so a 512 MB buffer is written between timed steps (outside the timed
 window) and every step starts cold.  Further lines in "workloads": the bf16
 variant, the fused-epilogue GEMM (8192 x 8192 x 4096, relu(scale*AB+bias)+R)
@@ -161,6 +164,12 @@ def max_over_ranks(x: float, world: int) -> float:
                      device="cuda" if torch.cuda.is_available() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(world: int, flops_per_step: float, steps: int, max_total_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank runs the same replica, so the job did
+    world x steps GEMMs in the slowest rank's time."""
+    return world * flops_per_step * steps / (max_total_ms * 1e-3) / 1e12
 
 
 def barrier(world: int):
@@ -333,6 +342,9 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
 
     import torch
@@ -371,7 +383,7 @@ def main():
         raise RuntimeError(f"device watchdog fired during the bench: {code:#x}")
     total_ms = max_over_ranks(sum(times), world)
     ms = total_ms / args.steps
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_value(world, flops, args.steps, total_ms)
     peak = float(peaks.get("bf16_tflops", 1900.0))  # dense fp16 rate equals bf16's
     achieved = flops / (statistics.mean(times) * 1e-3) / 1e12
     traffic = profiled_traffic(args.workload)
