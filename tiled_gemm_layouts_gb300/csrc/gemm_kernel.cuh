@@ -14,9 +14,15 @@
 //               instruction) into a double-buffered fp32 accumulator.
 //   warps 2..5  epilogue: tcgen05.ld 32x32b (thread t of warp w holds TMEM
 //               lane 32*(w%4)+t = tile row, register j = tile column), applies
-//               the epilogue in fp32 and stores with per-element edge masks,
-//               while the next tile's main loop already runs in the other
-//               accumulator buffer.
+//               the epilogue in fp32, stages each 32 x 32 output chunk in
+//               swizzled shared memory and writes it with a TMA tensor store
+//               (rows past M and columns past N clipped by the tensor map; a
+//               ragged last few columns stored directly), while the next
+//               tile's main loop already runs in the other accumulator buffer.
+// SK = true adds the stream-K tail: tiles of the last, part-empty wave are
+// cut into K-ranges dealt out to every worker; contributors publish fp32
+// partial sums to a caller workspace and the last to arrive adds them and
+// runs the epilogue.
 // PAIR = true runs each 256 x BN tile on a cluster of two CTAs with
 // tcgen05.mma.cta_group::2: CTA r holds rows 128r..128r+127 of the A block and
 // columns r*BN/2 .. (r+1)*BN/2-1 of the B block, so each SM stages half the
@@ -40,7 +46,7 @@ namespace tg {
 
 constexpr int kBK = 64;        // K elements per stage: one 128-byte swizzle row of fp16/bf16
 constexpr int kUmmaK = 16;     // K per tcgen05.mma of kind::f16
-constexpr int kEpiWarps = 4;   // one epilogue warp per TMEM lane quadrant (8 measured 7 % slower)
+constexpr int kEpiWarps = 4;   // one epilogue warp per TMEM lane quadrant (8 measured no faster overall)
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, epilogue warps
 constexpr int kStageBufs = 4;  // output staging buffers per epilogue warp
 
@@ -531,6 +537,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             uint32_t phase = 0;
             bool ok = true;
             int i = 0;
+            // One thread issues every MMA, so the instructions between two
+            // MMAs are on the critical path of the tensor pipe: the operand
+            // descriptors are built once here, and a K step or a stage step
+            // is a 32-bit add on their low words.  K-major operands step 16
+            // elements = 32 bytes inside the swizzle row (LBO unused);
+            // MN-major ones step 16 K-rows of 128 bytes, with LBO = 8 KB to
+            // the next 64-wide atom.
+            const uint32_t idesc = p.idesc;
+            const uint32_t d_hi = smem_desc_hi_sw128(1024);
+            const uint32_t a_lo0 = smem_desc_lo(smem_addr(sA), p.p_mn_major ? 8192u : 16u);
+            const uint32_t b_lo0 = smem_desc_lo(smem_addr(sB), p.q_mn_major ? 8192u : 16u);
+            const uint32_t a_kstep = p.p_mn_major ? (2048u >> 4) : (32u >> 4);
+            const uint32_t b_kstep = p.q_mn_major ? (2048u >> 4) : (32u >> 4);
             WorkIter items(p, worker);
             int t, kb0, kb1;
             for (; ok && items.next(t, kb0, kb1); ++i) {
@@ -545,20 +564,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_addr(sA + stage * TS::kAStage);
-                    const uint32_t b_addr = smem_addr(sB + stage * TS::kBStage);
+                    const uint32_t a_lo = a_lo0 + (uint32_t)stage * (TS::kAStage >> 4);
+                    const uint32_t b_lo = b_lo0 + (uint32_t)stage * (TS::kBStage >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                        // K-major: step 16 elements = 32 bytes inside the swizzle row.
-                        // MN-major: step 16 K-rows of 128 bytes.
-                        const uint64_t ad = p.p_mn_major
-                                                ? smem_desc_sw128(a_addr + kk * 2048, 8192, 1024)
-                                                : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-                        const uint64_t bd = p.q_mn_major
-                                                ? smem_desc_sw128(b_addr + kk * 2048, 8192, 1024)
-                                                : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-                        mma_f16<CG>(d_tmem, ad, bd, p.idesc, (kb != kb0) || (kk != 0));
-                    }
+                    for (int kk = 0; kk < kBK / kUmmaK; ++kk)
+                        mma_f16<CG>(d_tmem, smem_desc_join(a_lo + kk * a_kstep, d_hi),
+                                    smem_desc_join(b_lo + kk * b_kstep, d_hi), idesc,
+                                    (kb != kb0) || (kk != 0));
                     // frees the stage (in both CTAs) once the MMAs have read it
                     if constexpr (PAIR)
                         mma_commit_pair(smem_addr(&empty[stage]), 0x3);
