@@ -195,6 +195,7 @@ def workload_specs():
         # operand layouts: B stored N x K (K-major in shared memory), A stored K x M
         "fp16_4096_bT": dict(M=4096, N=4096, K=4096, dtype=S.F16, seed=1002, permB=1),
         "fp16_4096_aT": dict(M=4096, N=4096, K=4096, dtype=S.F16, seed=1002, permA=1),
+        "fp16_4096_aTbT": dict(M=4096, N=4096, K=4096, dtype=S.F16, seed=1002, permA=1, permB=1),
         # the fused epilogue's parts, for attributing its cost
         "fp16_8192x8192x4096_scale_bias_relu": dict(M=8192, N=8192, K=4096, dtype=S.F16,
                                                     seed=1003, bias=True, scale=True, relu=True),

@@ -111,8 +111,11 @@ def test_selector_reports_forced_configuration(tg):
 
 @pytest.mark.parametrize("force", CONFIGS)
 @pytest.mark.parametrize("permA,permB", [(0, 0), (1, 1)])
-def test_every_tile_configuration(tg, force, permA, permB):
-    M, N, K = 184, 328, 264  # ragged against every tile; dense strides stay 16-byte units
+@pytest.mark.parametrize("M,N,K", [
+    (184, 328, 264),  # ragged against every tile; dense strides stay 16-byte units
+    (320, 448, 200),  # M, N whole 64-wide atoms (MN-major stages as one 3-D box), K ragged
+])
+def test_every_tile_configuration(tg, force, permA, permB, M, N, K):
     p = synthetic.gemm_problem(M, N, K, BF16, 31, permA=permA, permB=permB,
                                bias=True, scale=True, residual=True)
     p["relu"] = True

@@ -237,6 +237,28 @@ bool encode_operand(CUtensorMap* map, int dtype, const void* base, int64_t rows,
     return encode_2d(map, dtype, base, k, rows, ld, 64, box_rows);
 }
 
+// An MN-major operand whose per-CTA stage is `atoms` 64-wide swizzle atoms,
+// as one 3-D box: dims {64 contiguous elements, K, rows / 64} with strides
+// {ld, 64} elements, box {64, 64, atoms}.  The atoms land 8 KB apart, which
+// is the stage layout the MMA descriptors expect, and a stage takes one TMA
+// instruction instead of `atoms` (each instruction costs TMA throughput).
+// Only for `rows` a multiple of 64: dimension 0 always spans 64 elements, so
+// a partial last atom would read past the end of its row.
+bool encode_mn_atoms(CUtensorMap* map, int dtype, const void* base, int64_t rows, int64_t k,
+                     int64_t ld, uint32_t atoms) {
+    if (rows % 64 != 0 || atoms < 2 || atoms > 4) return false;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)k, (cuuint64_t)(rows / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
+    const cuuint32_t box[3] = {64, 64, atoms};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        dtype == TG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 uint32_t make_idesc(int dtype, bool p_mn, bool q_mn, int n, int m) {
     const uint32_t fmt = dtype == TG_BF16 ? 1u : 0u;
     return (1u << 4)                   // accumulator format: fp32
@@ -298,17 +320,23 @@ int gemm_impl(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t stre
     // Each CTA stages 128 rows of P and q_box columns of Q (half the tile's
     // columns when a CTA pair shares the tile).
     const int q_box = cfg.pair ? cfg.bn / 2 : cfg.bn;
+    const void* p_base = swap ? a.B : a.A;
+    const void* q_base = swap ? a.A : a.B;
+    const int64_t p_ld = swap ? a.ldb : a.lda, q_ld = swap ? a.lda : a.ldb;
     if (!swap) {
         p_mn = a.permA == TG_OP_T;  // A stored K x M
         q_mn = a.permB == TG_OP_N;  // B stored K x N
-        ok = encode_operand(&p.map_p, a.dtype, a.A, a.M, a.K, a.lda, p_mn, 128) &&
-             encode_operand(&p.map_q, a.dtype, a.B, a.N, a.K, a.ldb, q_mn, q_box);
     } else {
         p_mn = a.permB == TG_OP_N;  // P = B^T: rows n contiguous when B is K x N
         q_mn = a.permA == TG_OP_T;  // Q = A^T: columns m contiguous when A is K x M
-        ok = encode_operand(&p.map_p, a.dtype, a.B, a.N, a.K, a.ldb, p_mn, 128) &&
-             encode_operand(&p.map_q, a.dtype, a.A, a.M, a.K, a.lda, q_mn, q_box);
     }
+    // MN-major stages as one 3-D box where the tile's CTA offsets are whole
+    // atoms (P: 128 rows per CTA; Q: q_box columns per CTA), else 2-D boxes.
+    p.p_3d = p_mn && encode_mn_atoms(&p.map_p, a.dtype, p_base, p.Mk, a.K, p_ld, 2);
+    p.q_3d = q_mn && q_box % 64 == 0 &&
+             encode_mn_atoms(&p.map_q, a.dtype, q_base, p.Nk, a.K, q_ld, (uint32_t)(q_box / 64));
+    ok = (p.p_3d || encode_operand(&p.map_p, a.dtype, p_base, p.Mk, a.K, p_ld, p_mn, 128)) &&
+         (p.q_3d || encode_operand(&p.map_q, a.dtype, q_base, p.Nk, a.K, q_ld, q_mn, q_box));
     // C for the epilogue's tensor stores: 32 x 32 chunks, rows of 64 bytes.
     // A tensor store bounds the innermost dimension in 16-byte units, so the
     // map stops at N rounded down to 8 columns; the kernel stores the rest

@@ -487,7 +487,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         const uint32_t a_dst = smem_addr(sA + stage * TS::kAStage);
                         const uint32_t b_dst = smem_addr(sB + stage * TS::kBStage);
                         const int k0 = kb * kBK;
-                        if (p.p_mn_major) {
+                        if (p.p_3d) {
+                            if constexpr (PAIR)
+                                tma_load_3d_pair(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
+                            else
+                                tma_load_3d(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
+                        } else if (p.p_mn_major) {
 #pragma unroll
                             for (int j = 0; j < 2; ++j) {
                                 if constexpr (PAIR)
@@ -501,7 +506,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                             else
                                 tma_load_2d(a_dst, &p.map_p, fb, k0, m0);
                         }
-                        if (p.q_mn_major) {
+                        if (p.q_3d) {
+                            if constexpr (PAIR)
+                                tma_load_3d_pair(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
+                            else
+                                tma_load_3d(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
+                        } else if (p.q_mn_major) {
 #pragma unroll
                             for (int j = 0; j < TS::kBBoxes; ++j) {
                                 if constexpr (PAIR)

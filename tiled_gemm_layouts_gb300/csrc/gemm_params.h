@@ -30,6 +30,7 @@ struct alignas(128) GemmParams {
     uint32_t idesc;      // tcgen05 instruction descriptor (dtype, majors, N, M)
     int p_mn_major;      // 1: P tile stored MN-major in shared memory
     int q_mn_major;
+    int p_3d, q_3d;      // 1: an MN-major stage arrives as one 3-D box (all its 64-wide atoms)
     int swap;            // 1: D is C^T
     int bf16;            // element type of every operand: 0 fp16, 1 bf16
     // epilogue, in C's (m, n) coordinates
