@@ -86,32 +86,20 @@ __device__ __forceinline__ void raise_abort(const Watch& w, int code) {
     atomicCAS(w.status, 0, code);
 }
 
+// Longest a waiting thread stays suspended inside one try_wait before it
+// checks the abort flag and its time limit again.
+constexpr uint32_t kSuspendNs = 200000;
+
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or
 // this wait ran out of time (then it raises the abort flags and records `code`).
+// The thread sleeps in the try_wait until the phase completes (or for at most
+// kSuspendNs), so it takes no issue slots or shared-memory bandwidth while it
+// waits.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Watch& w, int code) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*w.abort) return false;
-        if (clock64() - t0 > w.timeout) {
-            raise_abort(w, code);
-            return false;
-        }
-    }
-}
-
-// wait_bar for a wait expected to last a whole main loop (the epilogue's
-// wait for its accumulator): backs off between polls so the spinning lane
-// does not take issue slots from the producer and MMA warps that share its
-// SM sub-partition.
-__device__ __forceinline__ bool wait_bar_patient(uint32_t bar, uint32_t parity, const Watch& w,
-                                                 int code) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (true) {
-        __nanosleep(256);
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
         if (*w.abort) return false;
         if (clock64() - t0 > w.timeout) {
             raise_abort(w, code);
@@ -123,7 +111,7 @@ __device__ __forceinline__ bool wait_bar_patient(uint32_t bar, uint32_t parity, 
 // Bounded wait used while draining after an abort: ignores the abort flag.
 __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, const Watch& w) {
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_suspend(bar, parity, kSuspendNs)) {
         if (clock64() - t0 > w.timeout) return;
     }
 }
@@ -632,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             Aux cur, nxt;
             bool cur_full = (AUX && whole) ? prefetch_aux(p, rk, tn * BN + c_begin * 32, cur) : false;
             int ok = 1;
-            if (lane == 0) ok = wait_bar_patient(smem_addr(&tfull[buf]), aph, w, DEV_TIMEOUT_EPILOGUE);
+            if (lane == 0) ok = wait_bar(smem_addr(&tfull[buf]), aph, w, DEV_TIMEOUT_EPILOGUE);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             ok = epilogue_sync_and(ok);  // all four warps continue, or all stop
             if (!ok) break;
