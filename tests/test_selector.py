@@ -46,7 +46,7 @@ def test_invariants(tg, seed):
         assert c["grid"] % 2 == 0 and c["grid"] // 2 <= c["tiles"]
     else:
         assert c["grid"] <= c["tiles"]
-    assert c["stages"] >= 4 and 1 <= c["group_m"] <= 8
+    assert c["stages"] >= 4 and 1 <= c["group_m"] <= 16
     q_mn = (pa == 1) if c["swap"] else (pb == 0)
     assert not (c["bn"] == 32 and q_mn)
     assert c["swap"] == (1 if (M <= 64 and N > M) else 0)
