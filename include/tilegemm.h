@@ -252,6 +252,33 @@ int tg_layout_sublayout(const tg_layout* l, int n_in, const char* const* in_name
 int tg_layout_transpose_outs(const tg_layout* l, int n_out, const char* const* out_names,
                              tg_layout** out);
 
+/* Same map with the input dims reordered (transposeIns); in_names must name
+ * every input dim once. */
+int tg_layout_transpose_ins(const tg_layout* l, int n_in, const char* const* in_names,
+                            tg_layout** out);
+
+/* reshapeIns / reshapeOuts (section "Combining layouts": they "reorganize
+ * named dimensions and their bits"; the page gives no further definition).
+ * Reading taken: the input (output) bits are flattened with the first dim
+ * least significant and regrouped, in order, into the new dims of the given
+ * log2 sizes, whose total must equal the old total.  So the flattened input
+ * index keeps its value and so does the flattened output coordinate.
+ * TG_ERR_LAYOUT on a different total, a duplicate name or a size outside
+ * 0..30. */
+int tg_layout_reshape_ins(const tg_layout* l, int n_in, const char* const* in_names,
+                          const int* in_bits, tg_layout** out);
+int tg_layout_reshape_outs(const tg_layout* l, int n_out, const char* const* out_names,
+                           const int* out_bits, tg_layout** out);
+
+/* divideLeft / divideRight (section "Combining layouts": they "factor
+ * compatible layouts"; no further definition on the page).  Reading taken:
+ * the inverses of tg_layout_product.  divide_left returns C with
+ * A = B * C and divide_right returns C with A = C * B, equal as maps once
+ * dims are matched by name.  C has A's dims in A's order, each with A's bits
+ * less B's.  TG_ERR_LAYOUT when B is not such a factor of A. */
+int tg_layout_divide_left(const tg_layout* A, const tg_layout* B, tg_layout** out);
+int tg_layout_divide_right(const tg_layout* A, const tg_layout* B, tg_layout** out);
+
 /* Rank of the GF(2) matrix by row reduction; injective iff rank = total input
  * bits, surjective iff rank = total output bits (section "Surjectivity,
  * injectivity, and broadcasts").  Results in *value. */

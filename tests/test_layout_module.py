@@ -236,3 +236,125 @@ def test_invariant_violations_rejected(tg):
     a = tg.LinearLayout.create([("a", 1)], [("x", 2)], {"a": [(1,)]})
     with pytest.raises(tg.TileGemmError):  # out dims of inner != in dims of outer
         a.compose(a)
+
+
+# --- transposeIns, reshapeIns / reshapeOuts, divideLeft / divideRight ------
+# (Triton LinearLayout, "Combining layouts".  The page only names them; the
+# readings taken are stated in include/tilegemm.h.  Each test checks the
+# result by evaluating every input with the layout oracle.)
+
+def flat(dims, values):
+    """Flattened index of a dims-ordered coordinate, first dim least significant."""
+    v, shift = 0, 0
+    for (_, b), x in zip(dims, values):
+        v |= x << shift
+        shift += b
+    return v
+
+
+def split(dims, f):
+    out, shift = [], 0
+    for _, b in dims:
+        out.append((f >> shift) & ((1 << b) - 1))
+        shift += b
+    return out
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_transpose_ins_keeps_the_map(tg, seed):
+    rng = np.random.default_rng(4000 + seed)
+    L = random_layout(tg, rng, [int(rng.integers(0, 4)) for _ in range(3)], [3, 2])
+    order = [("a", "b", "c"), ("c", "a", "b"), ("b", "c", "a")][seed % 3]
+    T = L.transpose_ins(list(order))
+    assert [n for n, _ in T.in_dims] == list(order)
+    assert dict(T.in_dims) == dict(L.in_dims) and T.out_dims == L.out_dims
+    TL = tuple_of(L)
+    same_table(T, lambda x: lo.apply(TL, x))
+    with pytest.raises(tg.TileGemmError):
+        L.transpose_ins(["a", "b"])  # must name every dim
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_reshape_ins_keeps_the_flattened_index(tg, seed):
+    rng = np.random.default_rng(5000 + seed)
+    bits = [int(rng.integers(1, 4)) for _ in range(3)]
+    L = random_layout(tg, rng, bits, [3, 3])
+    total = sum(bits)
+    cut = int(rng.integers(0, total + 1))
+    new = [("p", cut), ("q", total - cut)]
+    R = L.reshape_ins(new)
+    assert R.in_dims == new and R.out_dims == L.out_dims
+    TL, TR = tuple_of(L), tuple_of(R)
+    for f in range(1 << total):
+        old_x = dict(zip([n for n, _ in TL[0]], split(TL[0], f)))
+        new_x = dict(zip([n for n, _ in TR[0]], split(TR[0], f)))
+        assert R.apply(new_x) == lo.apply(TL, old_x), f
+    with pytest.raises(tg.TileGemmError):
+        L.reshape_ins([("p", total + 1)])
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_reshape_outs_keeps_the_flattened_coordinate(tg, seed):
+    rng = np.random.default_rng(6000 + seed)
+    L = random_layout(tg, rng, [2, 3], [2, 3, 2], names=("a", "b"))
+    new = [("flat", 7)] if seed % 2 else [("lo", 4), ("hi", 3)]
+    R = L.reshape_outs(new)
+    assert R.out_dims == new and R.in_dims == L.in_dims
+    TL = tuple_of(L)
+    for x in lo.all_inputs(TL):
+        assert flat(new, R.apply(x)) == flat(TL[1], lo.apply(TL, x))
+    with pytest.raises(tg.TileGemmError):
+        L.reshape_outs([("flat", 6)])
+
+
+def product_by_rule(TB, TC, x, A_dims):
+    """(B * C)(x) written out from the product rule: for a dim both factors
+    have, B owns the low input bits and the low output bits."""
+    in_b, in_c = dict(TB[0]), dict(TC[0])
+    xb = {n: x[n] & ((1 << b) - 1) for n, b in in_b.items()}
+    xc = {n: x[n] >> in_b.get(n, 0) for n in in_c}
+    ob = dict(zip([n for n, _ in TB[1]], lo.apply(TB, xb)))
+    oc = dict(zip([n for n, _ in TC[1]], lo.apply(TC, xc)))
+    out_b = dict(TB[1])
+    return tuple(ob.get(n, 0) | (oc.get(n, 0) << out_b.get(n, 0)) for n, _ in A_dims)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_divide_left_and_right_invert_the_product(tg, seed):
+    rng = np.random.default_rng(7000 + seed)
+    # B: (a, b) -> (o0, o1); C: (b, c) -> (o1, o2), sharing input b and output o1
+    B = random_layout(tg, rng, [int(rng.integers(0, 3)), int(rng.integers(1, 3))], [2, 2],
+                      names=("a", "b"))
+    cin = [("b", int(rng.integers(0, 3))), ("c", int(rng.integers(1, 3)))]
+    cout = [("o1", 2), ("o2", 2)]
+    C = tg.LinearLayout.create(cin, cout, {n: [tuple(int(rng.integers(0, 4)) for _ in cout)
+                                               for _ in range(b)] for n, b in cin})
+    # left: A = B * C
+    A = B * C
+    TB, TC, TA = tuple_of(B), tuple_of(C), tuple_of(A)
+    for x in lo.all_inputs(TA):  # the product itself, by the rule
+        assert lo.apply(TA, x) == product_by_rule(TB, TC, x, TA[1])
+    Cl = A.divide_left(B)
+    assert [n for n, _ in Cl.in_dims] == [n for n, _ in A.in_dims]
+    TCl = tuple_of(Cl)
+    for x in lo.all_inputs(TA):
+        assert lo.apply(TA, x) == product_by_rule(TB, TCl, x, TA[1])
+    # right: A2 = C * B, divided by B on the right gives back C's map
+    A2 = C * B
+    Cr = A2.divide_right(B)
+    TA2, TCr = tuple_of(A2), tuple_of(Cr)
+    for x in lo.all_inputs(TA2):
+        assert lo.apply(TA2, x) == product_by_rule(TCr, TB, x, TA2[1])
+
+
+def test_divide_rejects_a_non_factor(tg):
+    B = tg.LinearLayout.create([("lane", 1)], [("x", 1)], {"lane": [(1,)]})
+    A = tg.LinearLayout.create([("lane", 2)], [("x", 2)], {"lane": [(2,), (1,)]})
+    with pytest.raises(tg.TileGemmError):  # A's low lane bit does not map as B's does
+        A.divide_left(B)
+    ok = tg.LinearLayout.create([("lane", 2)], [("x", 2)], {"lane": [(1,), (2,)]})
+    assert ok.divide_left(B).bases == {"lane": [(1,)]}
+    assert ok.divide_right(B).bases == {"lane": [(1,)]}
+    big = tg.LinearLayout.create([("lane", 3)], [("x", 1)], {"lane": [(1,), (0,), (0,)]})
+    with pytest.raises(tg.TileGemmError):  # B needs more output bits than A has left
+        tg.LinearLayout.create([("lane", 1)], [("x", 1)], {"lane": [(1,)]}).divide_left(big)

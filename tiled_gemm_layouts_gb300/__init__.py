@@ -89,6 +89,11 @@ _sig("tg_layout_compose", _int, _vp, _vp, _PP)
 _sig("tg_layout_product", _int, _vp, _vp, _PP)
 _sig("tg_layout_sublayout", _int, _vp, _int, ctypes.POINTER(_cp), _int, ctypes.POINTER(_cp), _PP)
 _sig("tg_layout_transpose_outs", _int, _vp, _int, ctypes.POINTER(_cp), _PP)
+_sig("tg_layout_transpose_ins", _int, _vp, _int, ctypes.POINTER(_cp), _PP)
+_sig("tg_layout_reshape_ins", _int, _vp, _int, ctypes.POINTER(_cp), ctypes.POINTER(_int), _PP)
+_sig("tg_layout_reshape_outs", _int, _vp, _int, ctypes.POINTER(_cp), ctypes.POINTER(_int), _PP)
+_sig("tg_layout_divide_left", _int, _vp, _vp, _PP)
+_sig("tg_layout_divide_right", _int, _vp, _vp, _PP)
 _sig("tg_layout_rank", _int, _vp, ctypes.POINTER(_int))
 _sig("tg_layout_is_injective", _int, _vp, ctypes.POINTER(_int))
 _sig("tg_layout_is_surjective", _int, _vp, ctypes.POINTER(_int))
@@ -108,7 +113,9 @@ EXPORTED = [
     "tg_probe_swizzle128", "tg_probe_tmem_32x32b", "tg_layout_create", "tg_layout_destroy",
     "tg_layout_num_dims", "tg_layout_in_dim", "tg_layout_out_dim", "tg_layout_get_bases",
     "tg_layout_apply", "tg_layout_compose", "tg_layout_product", "tg_layout_sublayout",
-    "tg_layout_transpose_outs", "tg_layout_rank", "tg_layout_is_injective",
+    "tg_layout_transpose_outs", "tg_layout_transpose_ins", "tg_layout_reshape_ins",
+    "tg_layout_reshape_outs", "tg_layout_divide_left", "tg_layout_divide_right",
+    "tg_layout_rank", "tg_layout_is_injective",
     "tg_layout_is_surjective", "tg_layout_invert_and_compose", "tg_layout_blocked",
     "tg_layout_cooperative", "tg_layout_register_tile", "tg_layout_swizzle128",
     "tg_layout_tmem_32x32b",
@@ -350,6 +357,30 @@ class LinearLayout:
     def transpose_outs(self, out_names) -> "LinearLayout":
         return self._new(_lib.tg_layout_transpose_outs, self._h, len(out_names),
                          _names(out_names), what="transpose_outs")
+
+    def transpose_ins(self, in_names) -> "LinearLayout":
+        return self._new(_lib.tg_layout_transpose_ins, self._h, len(in_names),
+                         _names(in_names), what="transpose_ins")
+
+    def reshape_ins(self, in_dims) -> "LinearLayout":
+        """in_dims: [(name, log2 size)] with the same total bits."""
+        bits = (_int * max(1, len(in_dims)))(*[b for _, b in in_dims])
+        return self._new(_lib.tg_layout_reshape_ins, self._h, len(in_dims),
+                         _names([n for n, _ in in_dims]), bits, what="reshape_ins")
+
+    def reshape_outs(self, out_dims) -> "LinearLayout":
+        """out_dims: [(name, log2 size)] with the same total bits."""
+        bits = (_int * max(1, len(out_dims)))(*[b for _, b in out_dims])
+        return self._new(_lib.tg_layout_reshape_outs, self._h, len(out_dims),
+                         _names([n for n, _ in out_dims]), bits, what="reshape_outs")
+
+    def divide_left(self, B: "LinearLayout") -> "LinearLayout":
+        """C with self = B * C."""
+        return self._new(_lib.tg_layout_divide_left, self._h, B._h, what="divide_left")
+
+    def divide_right(self, B: "LinearLayout") -> "LinearLayout":
+        """C with self = C * B."""
+        return self._new(_lib.tg_layout_divide_right, self._h, B._h, what="divide_right")
 
     def _int_query(self, fn):
         v = _int(0)

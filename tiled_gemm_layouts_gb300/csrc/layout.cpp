@@ -379,6 +379,165 @@ int tg_layout_transpose_outs(const tg_layout* l, int n_out, const char* const* o
     return tg_layout_sublayout(l, (int)ins.size(), ins.data(), n_out, out_names, out);
 }
 
+int tg_layout_transpose_ins(const tg_layout* l, int n_in, const char* const* in_names,
+                            tg_layout** out) {
+    if (!l || !out) return TG_ERR_INVALID_ARG;
+    if (n_in != (int)l->in_names.size()) return TG_ERR_LAYOUT;
+    std::vector<const char*> outs;
+    for (const auto& n : l->out_names) outs.push_back(n.c_str());
+    return tg_layout_sublayout(l, n_in, in_names, (int)outs.size(), outs.data(), out);
+}
+
+int tg_layout_reshape_ins(const tg_layout* l, int n_in, const char* const* in_names,
+                          const int* in_bits, tg_layout** out) {
+    if (!l || !out || (n_in > 0 && !in_bits)) return TG_ERR_INVALID_ARG;
+    return guarded([&] {
+        std::vector<int> ib(in_bits, in_bits + (n_in > 0 ? n_in : 0));
+        for (int b : ib)
+            if (b < 0) throw LayoutError();
+        if (total(ib) != total(l->in_bits)) throw LayoutError();
+        // the bases stay in flattened order: only the grouping into dims changes
+        tg_layout* r = make(names_of(n_in, in_names), ib, l->out_names, l->out_bits);
+        r->bases = l->bases;
+        try {
+            check(*r);
+        } catch (...) {
+            delete r;
+            throw;
+        }
+        *out = r;
+        return TG_OK;
+    });
+}
+
+int tg_layout_reshape_outs(const tg_layout* l, int n_out, const char* const* out_names,
+                           const int* out_bits, tg_layout** out) {
+    if (!l || !out || (n_out > 0 && !out_bits)) return TG_ERR_INVALID_ARG;
+    return guarded([&] {
+        std::vector<int> ob(out_bits, out_bits + (n_out > 0 ? n_out : 0));
+        for (int b : ob)
+            if (b < 0 || b > 30) throw LayoutError();
+        if (total(ob) != total(l->out_bits)) throw LayoutError();
+        tg_layout* r = make(l->in_names, l->in_bits, names_of(n_out, out_names), ob);
+        for (const auto& b : l->bases) {
+            const uint64_t f = flatten(*l, b);  // first out dim lowest
+            std::vector<int32_t> v;
+            int shift = 0;
+            for (int bits : ob) {
+                v.push_back((int32_t)((f >> shift) & ((1ull << bits) - 1)));
+                shift += bits;
+            }
+            r->bases.push_back(v);
+        }
+        try {
+            check(*r);
+        } catch (...) {
+            delete r;
+            throw;
+        }
+        *out = r;
+        return TG_OK;
+    });
+}
+
+}  // extern "C"
+
+namespace {
+
+// Whether P and A are the same map once their dims are matched by name.
+bool same_map(const tg_layout& P, const tg_layout& A) {
+    if (P.in_names.size() != A.in_names.size() || P.out_names.size() != A.out_names.size())
+        return false;
+    std::vector<int> out_of_p;  // P's out dim for each of A's
+    for (size_t o = 0; o < A.out_names.size(); ++o) {
+        const int k = find(P.out_names, A.out_names[o]);
+        if (k < 0 || P.out_bits[k] != A.out_bits[o]) return false;
+        out_of_p.push_back(k);
+    }
+    for (size_t d = 0; d < A.in_names.size(); ++d) {
+        const int k = find(P.in_names, A.in_names[d]);
+        if (k < 0 || P.in_bits[k] != A.in_bits[d]) return false;
+        const int pa = offset_of(A.in_bits, (int)d), pp = offset_of(P.in_bits, k);
+        for (int i = 0; i < A.in_bits[d]; ++i)
+            for (size_t o = 0; o < A.out_names.size(); ++o)
+                if (P.bases[pp + i][out_of_p[o]] != A.bases[pa + i][o]) return false;
+    }
+    return true;
+}
+
+// divideLeft (A = B * C) and divideRight (A = C * B) under the product's
+// convention that, for a dim both factors have, the left factor owns the low
+// input bits and the low output bits.  C keeps A's dims and order, each with
+// A's bits less B's.
+int divide(const tg_layout* A, const tg_layout* B, bool left, tg_layout** out) {
+    if (!A || !B || !out) return TG_ERR_INVALID_ARG;
+    return guarded([&] {
+        for (const auto& n : B->in_names)
+            if (find(A->in_names, n) < 0) throw LayoutError();
+        for (const auto& n : B->out_names)
+            if (find(A->out_names, n) < 0) throw LayoutError();
+        std::vector<int> b_in(A->in_names.size(), 0), c_in, b_out(A->out_names.size(), 0), c_out;
+        for (size_t d = 0; d < A->in_names.size(); ++d) {
+            const int k = find(B->in_names, A->in_names[d]);
+            if (k >= 0) b_in[d] = B->in_bits[k];
+            if (b_in[d] > A->in_bits[d]) throw LayoutError();
+            c_in.push_back(A->in_bits[d] - b_in[d]);
+        }
+        for (size_t o = 0; o < A->out_names.size(); ++o) {
+            const int k = find(B->out_names, A->out_names[o]);
+            if (k >= 0) b_out[o] = B->out_bits[k];
+            if (b_out[o] > A->out_bits[o]) throw LayoutError();
+            c_out.push_back(A->out_bits[o] - b_out[o]);
+        }
+        tg_layout* C = make(A->in_names, c_in, A->out_names, c_out);
+        try {
+            for (size_t d = 0; d < A->in_names.size(); ++d) {
+                const int base = offset_of(A->in_bits, (int)d);
+                const int first = left ? b_in[d] : 0;  // C's bits of this dim
+                for (int i = first; i < first + c_in[d]; ++i) {
+                    std::vector<int32_t> v;
+                    for (size_t o = 0; o < A->out_names.size(); ++o) {
+                        const int32_t c = A->bases[base + i][o];
+                        if (left) {  // C's coordinates sit above B's
+                            if (c & ((1 << b_out[o]) - 1)) throw LayoutError();
+                            v.push_back(c >> b_out[o]);
+                        } else {     // C's coordinates sit below B's
+                            if (c >> c_out[o]) throw LayoutError();
+                            v.push_back(c);
+                        }
+                    }
+                    C->bases.push_back(v);
+                }
+            }
+            check(*C);
+            // B's part of A must be B itself: rebuild the product and compare.
+            tg_layout* P = nullptr;
+            const int rc = left ? tg_layout_product(B, C, &P) : tg_layout_product(C, B, &P);
+            if (rc != TG_OK) throw LayoutError();
+            const bool same = same_map(*P, *A);
+            delete P;
+            if (!same) throw LayoutError();
+        } catch (...) {
+            delete C;
+            throw;
+        }
+        *out = C;
+        return TG_OK;
+    });
+}
+
+}  // namespace
+
+extern "C" {
+
+int tg_layout_divide_left(const tg_layout* A, const tg_layout* B, tg_layout** out) {
+    return divide(A, B, true, out);
+}
+
+int tg_layout_divide_right(const tg_layout* A, const tg_layout* B, tg_layout** out) {
+    return divide(A, B, false, out);
+}
+
 int tg_layout_rank(const tg_layout* l, int* value) {
     if (!l || !value) return TG_ERR_INVALID_ARG;
     *value = reduce(*l).rank;
