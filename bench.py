@@ -46,8 +46,13 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources that define the GEMM kernel, its launch and its
+    tile selection (not the host layout module or the probes)."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "tiled_gemm_layouts_gb300", "csrc", "*"))):
+    csrc = os.path.join(ROOT, "tiled_gemm_layouts_gb300", "csrc")
+    files = [f for f in glob.glob(os.path.join(csrc, "*"))
+             if os.path.basename(f).startswith(("gemm_", "api.", "select.", "ptx."))]
+    for f in sorted(files):
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode() + fh.read())
     return h.hexdigest()[:16]
