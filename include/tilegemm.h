@@ -28,7 +28,8 @@ enum {
     TG_OK = 0,
     TG_ERR_INVALID_ARG = 1,        /* null pointer, size <= 0 or > 2^31-1, bad enum, relu not 0/1 */
     TG_ERR_STRIDE = 2,             /* leading dimension < row width (or <= 0) */
-    TG_ERR_ALIGN = 3,              /* pointer not 16-byte aligned, or ld*2 bytes not a multiple of 16 */
+    TG_ERR_ALIGN = 3,              /* pointer not 16-byte aligned or ld*2 not a multiple of 16 (tg_gemm),
+                                      or a pointer not 2-byte aligned (every call) */
     TG_ERR_OVERLAP = 4,            /* output bytes intersect an input's bytes */
     TG_ERR_DTYPE = 5,              /* dtype not TG_F16 / TG_BF16 */
     TG_ERR_UNSUPPORTED_DEVICE = 6, /* no CUDA device, or not compute capability 10.x with tcgen05 */
@@ -111,6 +112,15 @@ int tg_gemm(int64_t M, int64_t N, int64_t K,
  *   call leaves its counters at zero again.  After TG_ERR_TIMEOUT from
  *   tg_debug_status, zero it again.  Calls that share a workspace must not
  *   run concurrently on the GPU.
+ * Unaligned operands: unlike tg_gemm, any pointer that is 2-byte aligned
+ *   and any positive stride are accepted (ninetoothed.org "Named layouts",
+ *   section "Runtime and compilation": positive, possibly non-contiguous
+ *   strides).  An operand a tensor map cannot describe (base not 16-byte
+ *   aligned, or ld*2 not a multiple of 16) is copied into an aligned dense
+ *   buffer inside the workspace first (A, B, R, bias, scale), and an
+ *   unaligned C is written to one and copied out afterwards: up to three
+ *   more kernel launches on `stream`, and workspace for the copies, as
+ *   tg_gemm_workspace_size_ex() reports.
  * workspace == NULL: exactly tg_gemm.  Other arguments, checks and errors as
  * tg_gemm; TG_ERR_BUFFER if workspace_bytes is too small, TG_ERR_ALIGN /
  * TG_ERR_OVERLAP / TG_ERR_POINTER for a misplaced workspace.
@@ -151,9 +161,19 @@ int tg_gemm_static_ws(int64_t M, int64_t N, int64_t K,
                       const tg_epilogue* epi, cudaStream_t stream);
 
 /* Workspace bytes tg_gemm_ws needs for these arguments on the current device
- * (0 when every tile is computed whole). */
+ * when every operand is aligned (0 when every tile is computed whole). */
 int tg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, tg_dtype dtype, tg_perm permA,
                            tg_perm permB, const tg_epilogue* epi, size_t* bytes);
+
+/* Workspace bytes tg_gemm_ws needs for exactly these arguments: the split's
+ * scratch plus a dense 16-byte-aligned copy (rows x round-up(width, 8)
+ * elements, each rounded to 256 bytes) of every operand a tensor map cannot
+ * describe.  The pointers are only inspected, never dereferenced.  Errors as
+ * tg_gemm's argument checks. */
+int tg_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                              tg_perm permA, const void* B, int64_t ldb, tg_perm permB,
+                              const void* C, int64_t ldc, tg_dtype dtype,
+                              const tg_epilogue* epi, size_t* bytes);
 
 /* Static name of a status code ("TG_OK", "TG_ERR_ALIGN", ...). */
 const char* tg_status_string(int status);

@@ -70,7 +70,8 @@ def test_valid_arguments_reach_device_check(tg):
     (dict(ldb=0), "TG_ERR_STRIDE"),
     (dict(pb=T_, K=512, ldb=504), "TG_ERR_STRIDE"),     # permuted B: ldb < K
     (dict(ldc=248), "TG_ERR_STRIDE"),                   # ldc < N: rows would overlap
-    (dict(A=FAKE + 2), "TG_ERR_ALIGN"),
+    (dict(A=FAKE + 2), "TG_ERR_ALIGN"),                 # tg_gemm: 16-byte bases only
+    (dict(B=FAKE + (1 << 30) + 1), "TG_ERR_ALIGN"),     # an odd byte address: never valid
     (dict(C=FAKE + (2 << 30) + 8), "TG_ERR_ALIGN"),
     (dict(lda=260), "TG_ERR_ALIGN"),                    # 520-byte rows
     (dict(K=250, lda=250), "TG_ERR_ALIGN"),
@@ -129,3 +130,16 @@ def test_package_fails_loudly_without_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", "import tiled_gemm_layouts_gb300"], cwd=tmp_path,
                        capture_output=True, text=True)
     assert r.returncode != 0 and "libtilegemm.so not found" in r.stderr
+
+
+def test_workspace_call_accepts_unaligned_operands_before_the_device_check(tg):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("device present: covered by tests/test_unaligned_gpu.py")
+    ws = FAKE + (3 << 30)
+    rc = tg.tg_gemm_ws(256, 256, 250, FAKE + 2, 250, N_, FAKE + (1 << 30), 256, N_,
+                       FAKE + (2 << 30) + 6, 257, F16, None, ws, 1 << 24)
+    assert rc == tg.TG_ERR_UNSUPPORTED_DEVICE  # the arguments passed every check
+    rc = tg.tg_gemm(256, 256, 250, FAKE + 2, 250, N_, FAKE + (1 << 30), 256, N_,
+                    FAKE + (2 << 30) + 6, 257, F16, None)
+    assert rc == tg.TG_ERR_ALIGN

@@ -167,12 +167,10 @@ int check_args(const Args& a) {
         a.ldc > kMaxLd)
         return TG_ERR_STRIDE;
     if (a.resid && (a.ldr < a.N || a.ldr > kMaxLd)) return TG_ERR_STRIDE;
-    if (!aligned16(a.A) || !aligned16(a.B) || !aligned16(a.C) || (a.lda * 2) % 16 ||
-        (a.ldb * 2) % 16 || (a.ldc * 2) % 16)
+    // every pointer addresses whole 16-bit elements
+    auto odd = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) != 0; };
+    if (odd(a.A) || odd(a.B) || odd(a.C) || odd(a.bias) || odd(a.scale) || odd(a.resid))
         return TG_ERR_ALIGN;
-    if ((a.bias && !aligned16(a.bias)) || (a.scale && !aligned16(a.scale)))
-        return TG_ERR_ALIGN;
-    if (a.resid && (!aligned16(a.resid) || (a.ldr * 2) % 16)) return TG_ERR_ALIGN;
     const Span c = span_of(a.C, a.M, a.N, a.ldc);
     const Span ins[5] = {span_of(a.A, a_rows, a_w, a.lda), span_of(a.B, b_rows, b_w, a.ldb),
                          span_of(a.bias, 1, a.N, a.N), span_of(a.scale, 1, a.M, a.M),
@@ -269,40 +267,124 @@ uint32_t make_idesc(int dtype, bool p_mn, bool q_mn, int n, int m) {
 
 }  // namespace
 
-int gemm_impl(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t stream) {
-    int rc = check_shape(a.M, a.N, a.K, a.dtype, a.permA, a.permB, nullptr);
+cudaError_t launch_copy_rows(const void* src, long long lds, void* dst, long long ldd,
+                             long long rows, long long cols, cudaStream_t stream);
+
+// Operands a tensor map cannot describe (base not 16-byte aligned, or a row
+// stride that is not a whole number of 16-byte units) are staged through the
+// caller's workspace: copied into aligned dense buffers (A, B, R, bias,
+// scale), or, for C, written to one and copied out after the GEMM.
+struct Staging {
+    bool A = false, B = false, C = false, R = false, bias = false, scale = false;
+    size_t bytes = 0;  // staging buffers, each rounded to 256 bytes
+    bool any() const { return A || B || C || R || bias || scale; }
+};
+
+int64_t up8(int64_t x) { return (x + 7) / 8 * 8; }
+size_t dense_bytes(int64_t rows, int64_t width) {
+    return ((size_t)rows * (size_t)up8(width) * 2 + 255) / 256 * 256;
+}
+
+Staging staging_of(const Args& a) {
+    Staging s;
+    const int64_t a_rows = a.permA == TG_OP_N ? a.M : a.K, a_w = a.permA == TG_OP_N ? a.K : a.M;
+    const int64_t b_rows = a.permB == TG_OP_N ? a.K : a.N, b_w = a.permB == TG_OP_N ? a.N : a.K;
+    s.A = !aligned16(a.A) || (a.lda * 2) % 16;
+    s.B = !aligned16(a.B) || (a.ldb * 2) % 16;
+    s.C = !aligned16(a.C) || (a.ldc * 2) % 16;
+    s.R = a.resid && (!aligned16(a.resid) || (a.ldr * 2) % 16);
+    s.bias = a.bias && !aligned16(a.bias);
+    s.scale = a.scale && !aligned16(a.scale);
+    if (s.A) s.bytes += dense_bytes(a_rows, a_w);
+    if (s.B) s.bytes += dense_bytes(b_rows, b_w);
+    if (s.C) s.bytes += dense_bytes(a.M, a.N);
+    if (s.R) s.bytes += dense_bytes(a.M, a.N);
+    if (s.bias) s.bytes += dense_bytes(1, a.N);
+    if (s.scale) s.bytes += dense_bytes(1, a.M);
+    return s;
+}
+
+size_t split_bytes(const KernelConfig& cfg) {
+    return cfg.sk_tiles > 0 ? ((size_t)cfg.ws_bytes + 255) / 256 * 256 : 0;
+}
+
+int gemm_impl(const Args& user, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    int rc = check_shape(user.M, user.N, user.K, user.dtype, user.permA, user.permB, nullptr);
     if (rc) return rc;
-    if (a.relu != 0 && a.relu != 1) return TG_ERR_INVALID_ARG;
-    if ((rc = check_args(a))) return rc;
+    if (user.relu != 0 && user.relu != 1) return TG_ERR_INVALID_ARG;
+    if ((rc = check_args(user))) return rc;
+    const Staging st = staging_of(user);
+    if (st.any() && !workspace) return TG_ERR_ALIGN;  // staging needs the caller's workspace
     int dev;
     DeviceInfo* info;
     if ((rc = current_device(&dev, &info))) return rc;
     load_driver_entry_points();
     if (!g_encode) return TG_ERR_CUDA;
-    if ((rc = check_pointers(a, dev))) return rc;
+    if ((rc = check_pointers(user, dev))) return rc;
 
-    const KernelConfig cfg = select_config(a.M, a.N, a.K, a.dtype, a.permA, a.permB,
-                                           a.bias != nullptr || a.scale != nullptr ||
-                                               a.resid != nullptr || a.relu,
+    const KernelConfig cfg = select_config(user.M, user.N, user.K, user.dtype, user.permA,
+                                           user.permB,
+                                           user.bias != nullptr || user.scale != nullptr ||
+                                               user.resid != nullptr || user.relu,
                                            info->sms, workspace != nullptr);
-    if (cfg.sk_tiles > 0) {
+    const size_t sk_bytes = split_bytes(cfg), need = sk_bytes + st.bytes;
+    if (need > 0) {
         // The workspace is written: it must be device memory of this device,
         // large enough, and disjoint from every operand.
         if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TG_ERR_ALIGN;
-        if ((long long)ws_bytes < cfg.ws_bytes) return TG_ERR_BUFFER;
+        if (ws_bytes < need) return TG_ERR_BUFFER;
         Span ws;
         ws.present = true;
         ws.lo = reinterpret_cast<uintptr_t>(workspace);
-        ws.hi = (u128)ws.lo + (u128)cfg.ws_bytes;
-        const int64_t a_rows = a.permA == TG_OP_N ? a.M : a.K, a_w = a.permA == TG_OP_N ? a.K : a.M;
-        const int64_t b_rows = a.permB == TG_OP_N ? a.K : a.N, b_w = a.permB == TG_OP_N ? a.N : a.K;
-        const Span others[6] = {span_of(a.C, a.M, a.N, a.ldc), span_of(a.A, a_rows, a_w, a.lda),
-                                span_of(a.B, b_rows, b_w, a.ldb), span_of(a.bias, 1, a.N, a.N),
-                                span_of(a.scale, 1, a.M, a.M), span_of(a.resid, a.M, a.N, a.ldr)};
+        ws.hi = (u128)ws.lo + (u128)need;
+        const int64_t a_rows = user.permA == TG_OP_N ? user.M : user.K;
+        const int64_t a_w = user.permA == TG_OP_N ? user.K : user.M;
+        const int64_t b_rows = user.permB == TG_OP_N ? user.K : user.N;
+        const int64_t b_w = user.permB == TG_OP_N ? user.N : user.K;
+        const Span others[6] = {span_of(user.C, user.M, user.N, user.ldc),
+                                span_of(user.A, a_rows, a_w, user.lda),
+                                span_of(user.B, b_rows, b_w, user.ldb),
+                                span_of(user.bias, 1, user.N, user.N),
+                                span_of(user.scale, 1, user.M, user.M),
+                                span_of(user.resid, user.M, user.N, user.ldr)};
         for (const Span& o : others)
             if (intersects(ws, o)) return TG_ERR_OVERLAP;
         if ((rc = check_pointer(workspace, ws, dev))) return rc;
     }
+    // Stage what the tensor maps cannot describe (after the split's region).
+    Args staged = user;
+    if (st.any()) {
+        char* cursor = static_cast<char*>(workspace) + sk_bytes;
+        auto take = [&](int64_t rows, int64_t width, int64_t* ld) {
+            void* d = cursor;
+            *ld = up8(width);
+            cursor += dense_bytes(rows, width);
+            return d;
+        };
+        auto copy_in = [&](const void* src, int64_t lds, int64_t rows, int64_t width,
+                           const void** dst, int64_t* ldd) {
+            void* d = take(rows, width, ldd);
+            *dst = d;
+            return launch_copy_rows(src, lds, d, *ldd, rows, width, stream) == cudaSuccess;
+        };
+        const int64_t a_rows = user.permA == TG_OP_N ? user.M : user.K;
+        const int64_t a_w = user.permA == TG_OP_N ? user.K : user.M;
+        const int64_t b_rows = user.permB == TG_OP_N ? user.K : user.N;
+        const int64_t b_w = user.permB == TG_OP_N ? user.N : user.K;
+        int64_t unused = 0;
+        bool ok = true;
+        if (st.A) ok = ok && copy_in(user.A, user.lda, a_rows, a_w, &staged.A, &staged.lda);
+        if (st.B) ok = ok && copy_in(user.B, user.ldb, b_rows, b_w, &staged.B, &staged.ldb);
+        if (st.R) ok = ok && copy_in(user.resid, user.ldr, user.M, user.N, &staged.resid, &staged.ldr);
+        if (st.bias) ok = ok && copy_in(user.bias, user.N, 1, user.N, &staged.bias, &unused);
+        if (st.scale) ok = ok && copy_in(user.scale, user.M, 1, user.M, &staged.scale, &unused);
+        if (st.C) staged.C = take(user.M, user.N, &staged.ldc);
+        if (!ok) {
+            cudaGetLastError();
+            return TG_ERR_CUDA;
+        }
+    }
+    const Args& a = staged;
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
     const bool swap = cfg.swap != 0;
@@ -372,7 +454,9 @@ int gemm_impl(const Args& a, void* workspace, size_t ws_bytes, cudaStream_t stre
     p.timeout_cycles = g_timeout.load();
     p.status = info->status;
     p.inject_skip_load = (int)g_skip_kblock.load();
-    const cudaError_t e = launch_gemm(p, cfg, info->sms, stream);
+    cudaError_t e = launch_gemm(p, cfg, info->sms, stream);
+    if (e == cudaSuccess && st.C)  // the staged C out to the caller's
+        e = launch_copy_rows(staged.C, staged.ldc, user.C, user.ldc, user.M, user.N, stream);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_CUDA;
@@ -432,6 +516,41 @@ extern "C" int tg_gemm_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_
     a.ldr = (epi && epi->residual) ? (epi->ldr ? epi->ldr : ldc) : 0;
     a.relu = epi ? epi->relu : 0;
     return gemm_impl(a, workspace, workspace_bytes, stream);
+}
+
+extern "C" int tg_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const void* A,
+                                         int64_t lda, tg_perm permA, const void* B, int64_t ldb,
+                                         tg_perm permB, const void* C, int64_t ldc,
+                                         tg_dtype dtype, const tg_epilogue* epi, size_t* bytes) {
+    int rc = check_shape(M, N, K, (int)dtype, (int)permA, (int)permB, epi);
+    if (rc) return rc;
+    if (!bytes) return TG_ERR_INVALID_ARG;
+    Args a;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.A = A;
+    a.lda = lda;
+    a.permA = (int)permA;
+    a.B = B;
+    a.ldb = ldb;
+    a.permB = (int)permB;
+    a.C = const_cast<void*>(C);
+    a.ldc = ldc;
+    a.dtype = (int)dtype;
+    a.bias = epi ? epi->bias_n : nullptr;
+    a.scale = epi ? epi->scale_m : nullptr;
+    a.resid = epi ? epi->residual : nullptr;
+    a.ldr = (epi && epi->residual) ? (epi->ldr ? epi->ldr : ldc) : 0;
+    a.relu = epi ? epi->relu : 0;
+    if ((rc = check_args(a))) return rc;
+    int dev;
+    DeviceInfo* info;
+    if ((rc = current_device(&dev, &info))) return rc;
+    const KernelConfig c = select_config(M, N, K, (int)dtype, (int)permA, (int)permB,
+                                         a.bias || a.scale || a.resid || a.relu, info->sms, true);
+    *bytes = split_bytes(c) + staging_of(a).bytes;
+    return TG_OK;
 }
 
 extern "C" int tg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, tg_dtype dtype,

@@ -66,7 +66,8 @@ extern "C" int tg_gemm_static_ws(int64_t M, int64_t N, int64_t K, const void* A,
                                  void* C, int64_t ldc, tg_dtype dtype, const tg_epilogue* epi,
                                  cudaStream_t stream) {
     size_t need = 0;
-    int rc = tg_gemm_workspace_size(M, N, K, dtype, permA, permB, epi, &need);
+    int rc = tg_gemm_workspace_size_ex(M, N, K, A, lda, permA, B, ldb, permB, C, ldc, dtype, epi,
+                                       &need);
     if (rc != TG_OK) return rc;
     if (need > kScratchBytes) return TG_ERR_BUFFER;  // more scratch than the static array holds
     void* scratch = nullptr;
