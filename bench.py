@@ -266,6 +266,38 @@ class DeviceProblem:
                         stream)
 
 
+class DevicePointwise:
+    """Device-resident inputs and output of one pointwise program."""
+
+    def __init__(self, tg, p):
+        import numpy as np
+        import torch
+        self.p = p
+        self.tg = tg
+        dev = lambda a: None if a is None else torch.from_numpy(
+            np.ascontiguousarray(a).view(np.int16)).cuda()
+        self.X = dev(p["X"])
+        self.bias, self.scale, self.R = dev(p.get("bias")), dev(p.get("scale")), dev(p.get("R"))
+        self.C = torch.empty((p["M"], p["N"]), dtype=torch.int16, device="cuda")
+        self.epi = tg.make_epilogue(self.bias, self.scale, p.get("relu", False), self.R,
+                                    p.get("ldr", 0) or 0)
+
+    def call(self, stream):
+        p = self.p
+        rc = self.tg.tg_pointwise(p["M"], p["N"], self.X, p["ldx"], p["permX"], self.C, p["N"],
+                                  p["dtype"], self.epi, stream)
+        if rc != self.tg.TG_OK:
+            raise RuntimeError(self.tg.tg_status_string(rc))
+
+    def bytes(self) -> int:
+        p = self.p
+        n = 2 * p["M"] * p["N"] * 2  # X read, C written
+        if p.get("R") is not None:
+            n += 2 * p["M"] * p["N"]
+        n += 2 * p["N"] * (p.get("bias") is not None) + 2 * p["M"] * (p.get("scale") is not None)
+        return n
+
+
 def time_kernel(fn, steps, warmup, flush_buf, stream):
     """Per-step kernel times (ms) by CUDA events on the launching stream, L2
     flushed before every step outside the event window."""
@@ -467,6 +499,19 @@ def main():
             del dp
         fused, plain = others["fp16_8192x8192x4096_fused"], others["fp16_8192x8192x4096_plain"]
         others["fused_over_plain_time"] = fused["ms_median"] / plain["ms_median"]
+        import synthetic as S
+        for key, permX in (("pointwise_fp16_8192x8192_scale_bias_relu_residual", 0),
+                           ("pointwise_fp16_8192x8192_permuted_input", 1)):
+            pp = S.pointwise_problem(8192, 8192, S.F16, 1020 + permX, permX=permX,
+                                     bias=True, scale=True, residual=permX == 0)
+            pp["relu"] = True
+            dpw = DevicePointwise(tg, pp)
+            ts = time_kernel(dpw.call, 10, 3, flush, stream)
+            t = statistics.median(ts) * 1e-3
+            gbs = dpw.bytes() / t / 1e9
+            others[key] = {"gbs": gbs, "hbm_frac": gbs / float(peaks.get("hbm_gbs", 6800.0)),
+                           "ms_median": t * 1e3, "bytes": dpw.bytes()}
+            del dpw
         line["workloads"] = others
         if rank == 0:
             tfl, rows, secs, cores = oracle_sample_tflops(hp, args.cpu_seconds)

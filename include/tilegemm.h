@@ -175,6 +175,29 @@ int tg_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const void* A, in
                               const void* C, int64_t ldc, tg_dtype dtype,
                               const tg_epilogue* epi, size_t* bytes);
 
+/*
+ * Pointwise program of the named-layout pages (ninetoothed.org "Named
+ * layouts": pointwise work, missing-axis broadcasting, reordering and
+ * same-output-domain bias/ReLU/residual postprocessing):
+ *
+ *     C[m, n] = epilogue( X(m, n) )       (the tg_epilogue above, same order)
+ *
+ * scale_m has axes ("m") and bias_n axes ("n"): each broadcasts along the
+ * axis it lacks.  X(m, n) = X[m*ldx + n] with ldx >= N (permX = TG_OP_N), or
+ * X[n*ldx + m] with ldx >= M when the input is given permuted (TG_OP_T,
+ * storage N x M): an explicit permute, never inferred from sizes.
+ * C(m, n) = C[m*ldc + n], ldc >= N.  fp32 arithmetic, round to nearest even.
+ *
+ * Any positive strides and any 2-byte-aligned pointers (16-byte-aligned
+ * rows use vector accesses).  C's bytes must be disjoint from X, bias,
+ * scale and R; every pointer inside one device allocation of the current
+ * device.  One kernel launch on `stream`; nothing allocated.  Errors as
+ * tg_gemm's checks (TG_ERR_ALIGN only for an odd byte address).
+ */
+int tg_pointwise(int64_t M, int64_t N, const void* X, int64_t ldx, tg_perm permX,
+                 void* C, int64_t ldc, tg_dtype dtype, const tg_epilogue* epi,
+                 cudaStream_t stream);
+
 /* Static name of a status code ("TG_OK", "TG_ERR_ALIGN", ...). */
 const char* tg_status_string(int status);
 

@@ -6,6 +6,7 @@ shares no code with it.
 
 * ``gemm``: the fp64 plain-definition GEMM with the fused epilogue
   (``gemm_oracle.c``, compiled here with gcc + OpenMP).
+* ``pointwise``: the fp64 named-layout pointwise program (numpy, row by row).
 * ``layouts``: brute-force GF(2) layout evaluation and the pages' ownership
   rules written out directly (``layout_oracle.py``).
 """
@@ -85,4 +86,37 @@ def gemm(p: dict, rows: tuple[int, int] | None = None, relu: bool | None = None,
                              _ptr(arrs["R"]), p.get("ldr", 0) or 0, r0, r1, _ptr(y), threads)
     if rc != 0:
         raise ValueError("oracle_gemm rejected its arguments")
+    return y
+
+
+def pointwise(p: dict) -> np.ndarray:
+    """y(m, n) in fp64 of the named-layout pointwise program
+    (ninetoothed.org "Named layouts": pointwise work, missing-axis
+    broadcasting, reordering, bias/ReLU/residual postprocessing).
+
+    x = X(m, n), read through the explicit permute (permX = 0: X[m, n] of an
+    M x ldx buffer; permX = 1: X[n, m] of an N x ldx buffer), then the GEMM's
+    epilogue in its order: x *= scale_m[m]; x += bias_n[n]; x = max(x, 0);
+    x += R[m, n].  An absent operand is the identity; scale_m (axes "m") is
+    the same for every n of a row, bias_n (axes "n") the same for every m of
+    a column.  Unrounded.  ``p`` holds the keys of
+    ``synthetic.pointwise_problem``.
+    """
+    M, N, dt = p["M"], p["N"], p["dtype"]
+    X = decode(p["X"], dt)
+    bias = None if p.get("bias") is None else decode(p["bias"], dt)
+    scale = None if p.get("scale") is None else decode(p["scale"], dt)
+    R = None if p.get("R") is None else decode(p["R"], dt)
+    y = np.empty((M, N), dtype=np.float64)
+    for m in range(M):
+        row = X[m, :N].copy() if p["permX"] == 0 else X[:N, m].copy()
+        if scale is not None:
+            row *= scale[m]
+        if bias is not None:
+            row += bias[:N]
+        if p.get("relu", False):
+            row = np.maximum(row, 0.0)
+        if R is not None:
+            row += R[m, :N]
+        y[m] = row
     return y

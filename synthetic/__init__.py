@@ -142,3 +142,27 @@ def gemm_problem(M: int, N: int, K: int, dtype: int, seed: int, *, permA: int = 
         out["R"] = None
         out["ldr"] = 0
     return out
+
+
+def pointwise_problem(M: int, N: int, dtype: int, seed: int, *, permX: int = 0,
+                      ldx: int | None = None, dist: str = "uniform", sigma: float = 0.5,
+                      bias: bool = False, scale: bool = False, residual: bool = False,
+                      ldr: int | None = None) -> dict:
+    """Storage buffers for one pointwise program, drawn in the order X, bias,
+    scale, R.  permX = 0: X is an M x ldx buffer (X(m,n) = X[m, n]);
+    permX = 1: an N x ldx buffer holding the transpose (X(m,n) = X[n, m])."""
+    x_rows, x_w = (M, N) if permX == 0 else (N, M)
+    ldx = x_w if ldx is None else ldx
+    s = Stream(seed)
+    out = {"M": M, "N": N, "dtype": dtype, "permX": permX, "ldx": ldx}
+    out["X"] = s.matrix(x_rows, ldx, dtype, dist, sigma)
+    out["bias"] = s.vector(N, dtype, dist, sigma) if bias else None
+    out["scale"] = s.vector(M, dtype, dist, sigma) if scale else None
+    if residual:
+        ldr = N if ldr is None else ldr
+        out["R"] = s.matrix(M, ldr, dtype, dist, sigma)
+        out["ldr"] = ldr
+    else:
+        out["R"] = None
+        out["ldr"] = 0
+    return out

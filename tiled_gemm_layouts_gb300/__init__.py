@@ -69,6 +69,8 @@ _sig("tg_gemm_ws", _int, _i64, _i64, _i64, _vp, _i64, _int, _vp, _i64, _int, _vp
      ctypes.POINTER(tg_epilogue), _vp, ctypes.c_size_t, _vp)
 _sig("tg_gemm_workspace_size", _int, _i64, _i64, _i64, _int, _int, _int,
      ctypes.POINTER(tg_epilogue), ctypes.POINTER(ctypes.c_size_t))
+_sig("tg_pointwise", _int, _i64, _i64, _vp, _i64, _int, _vp, _i64, _int,
+     ctypes.POINTER(tg_epilogue), _vp)
 _sig("tg_gemm_workspace_size_ex", _int, _i64, _i64, _i64, _vp, _i64, _int, _vp, _i64, _int, _vp,
      _i64, _int, ctypes.POINTER(tg_epilogue), ctypes.POINTER(ctypes.c_size_t))
 _sig("tg_gemm_static_ws", _int, _i64, _i64, _i64, _vp, _i64, _int, _vp, _i64, _int, _vp, _i64,
@@ -109,6 +111,7 @@ _sig("tg_layout_tmem_32x32b", _int, _int, _PP)
 
 EXPORTED = [
     "tg_gemm", "tg_gemm_ws", "tg_gemm_workspace_size", "tg_gemm_workspace_size_ex",
+    "tg_pointwise",
     "tg_gemm_static_ws",
     "tg_status_string", "tg_query_config",
     "tg_query_config_ws", "tg_query_config_for_sms",
@@ -204,6 +207,11 @@ def tg_gemm_workspace_size(M, N, K, dtype, permA=TG_OP_N, permB=TG_OP_N, epi=Non
     if rc != TG_OK:
         raise TileGemmError(rc, "tg_gemm_workspace_size")
     return n.value
+
+
+def tg_pointwise(M, N, X, ldx, permX, C, ldc, dtype, epi=None, stream=None) -> int:
+    return _lib.tg_pointwise(M, N, _addr(X), ldx, permX, _addr(C), ldc, dtype,
+                             ctypes.byref(epi) if epi is not None else None, _stream(stream))
 
 
 def tg_gemm_workspace_size_ex(M, N, K, A, lda, permA, B, ldb, permB, C, ldc, dtype,

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtilegemm.so")
 
-CUDA_SOURCES = ["api.cu", "gemm_sm103.cu", "probes.cu", "noalloc.cu", "stage.cu"] + [f"gemm_inst_{i}.cu" for i in range(1, 37)]
+CUDA_SOURCES = ["api.cu", "gemm_sm103.cu", "probes.cu", "noalloc.cu", "stage.cu", "pointwise.cu"] + [f"gemm_inst_{i}.cu" for i in range(1, 37)]
 CXX_SOURCES = ["layout.cpp", "select.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

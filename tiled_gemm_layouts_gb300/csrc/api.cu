@@ -18,6 +18,7 @@
 
 #include "../../include/tilegemm.h"
 #include "gemm_params.h"
+#include "pointwise.h"
 #include "select.h"
 
 namespace tg {
@@ -516,6 +517,57 @@ extern "C" int tg_gemm_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_
     a.ldr = (epi && epi->residual) ? (epi->ldr ? epi->ldr : ldc) : 0;
     a.relu = epi ? epi->relu : 0;
     return gemm_impl(a, workspace, workspace_bytes, stream);
+}
+
+extern "C" int tg_pointwise(int64_t M, int64_t N, const void* X, int64_t ldx, tg_perm permX,
+                            void* C, int64_t ldc, tg_dtype dtype, const tg_epilogue* epi,
+                            cudaStream_t stream) {
+    if (M <= 0 || N <= 0 || M > kMaxDim || N > kMaxDim) return TG_ERR_INVALID_ARG;
+    if (permX != TG_OP_N && permX != TG_OP_T) return TG_ERR_INVALID_ARG;
+    if (epi && epi->relu != 0 && epi->relu != 1) return TG_ERR_INVALID_ARG;
+    if (dtype != TG_F16 && dtype != TG_BF16) return TG_ERR_DTYPE;
+    if (!X || !C) return TG_ERR_INVALID_ARG;
+    const void* bias = epi ? epi->bias_n : nullptr;
+    const void* scale = epi ? epi->scale_m : nullptr;
+    const void* resid = epi ? epi->residual : nullptr;
+    const int64_t ldr = resid ? (epi->ldr ? epi->ldr : ldc) : 0;
+    const int64_t x_rows = permX == TG_OP_N ? M : N, x_w = permX == TG_OP_N ? N : M;
+    constexpr int64_t kMaxLd = (1LL << 39) - 8;
+    if (ldx < x_w || ldc < N || ldx > kMaxLd || ldc > kMaxLd) return TG_ERR_STRIDE;
+    if (resid && (ldr < N || ldr > kMaxLd)) return TG_ERR_STRIDE;
+    auto odd = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) != 0; };
+    if (odd(X) || odd(C) || odd(bias) || odd(scale) || odd(resid)) return TG_ERR_ALIGN;
+    // output storage disjoint from every input (rows of C never overlap: ldc >= N)
+    const Span c = span_of(C, M, N, ldc);
+    if (intersects(c, span_of(X, x_rows, x_w, ldx)) || intersects(c, span_of(bias, 1, N, N)) ||
+        intersects(c, span_of(scale, 1, M, M)) || intersects(c, span_of(resid, M, N, ldr)))
+        return TG_ERR_OVERLAP;
+    int rc, dev;
+    DeviceInfo* info;
+    if ((rc = current_device(&dev, &info))) return rc;
+    load_driver_entry_points();  // the allocation-range query of check_pointer
+    if ((rc = check_pointer(X, span_of(X, x_rows, x_w, ldx), dev)) ||
+        (rc = check_pointer(C, c, dev)) || (rc = check_pointer(bias, span_of(bias, 1, N, N), dev)) ||
+        (rc = check_pointer(scale, span_of(scale, 1, M, M), dev)) ||
+        (rc = check_pointer(resid, span_of(resid, M, N, ldr), dev)))
+        return rc;
+    PwParams p;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.X = static_cast<const uint16_t*>(X);
+    p.ldx = ldx;
+    p.C = static_cast<uint16_t*>(C);
+    p.ldc = ldc;
+    p.scale = static_cast<const uint16_t*>(scale);
+    p.bias = static_cast<const uint16_t*>(bias);
+    p.R = static_cast<const uint16_t*>(resid);
+    p.ldr = ldr;
+    p.relu = epi ? epi->relu : 0;
+    if (launch_pointwise(p, permX == TG_OP_T, dtype == TG_BF16, info->sms, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_CUDA;
+    }
+    return TG_OK;
 }
 
 extern "C" int tg_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const void* A,
