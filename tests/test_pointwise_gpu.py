@@ -109,3 +109,24 @@ def test_argument_checks(tg):
     assert tg.tg_pointwise(64, 64, host, 64, 0, C, 64, F16) == tg.TG_ERR_POINTER
     assert tg.tg_pointwise(64, 64, X, 64, 0, C, 64, F16) == tg.TG_OK
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("epi", [{}, dict(bias=True, scale=True, relu=True, residual=True)])
+def test_permuted_input_with_aligned_rows(tg, dtype, epi):
+    # every row starts on a 16-byte boundary: the 16-byte-vector transpose
+    # path, with M and N ragged against its 64 x 64 tiles and 8-wide vectors
+    M, N = 1001, 700
+    flags = dict(epi)
+    relu = flags.pop("relu", False)
+    if flags.get("residual"):
+        flags["ldr"] = 704
+    p = synthetic.pointwise_problem(M, N, dtype, 31, permX=1, ldx=1008, **flags)
+    p["relu"] = relu
+    c, rc = run(tg, p, 704)
+    assert rc == tg.TG_OK
+    if not epi:
+        assert np.array_equal(c[:, :N], p["X"][:N, :M].T)
+    else:
+        check_close(c, oracle.pointwise(p), dtype, what="aligned permuted")
+    check_padding(c, N)

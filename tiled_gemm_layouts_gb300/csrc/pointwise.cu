@@ -161,6 +161,73 @@ __global__ void __launch_bounds__(256) pointwise_transposed_kernel(const PwParam
     }
 }
 
+// The same with 16-byte accesses, when X's rows, C's rows, R's rows and bias
+// all start on 16-byte boundaries: each thread moves two 8-element vectors
+// of storage rows in, and writes two 8-element vectors of C rows out.
+template <bool BF>
+__global__ void __launch_bounds__(256) pointwise_transposed_vec_kernel(const PwParams p) {
+    __shared__ float tile[64][65];  // [n - n0][m - m0]
+    const int t = threadIdx.x;
+    const int tiles_m = (p.M + 63) / 64, tiles_n = (p.N + 63) / 64;
+    const long long tiles = (long long)tiles_m * tiles_n;
+    for (long long u = blockIdx.x; u < tiles; u += gridDim.x) {
+        const int m0 = (int)(u % tiles_m) * 64, n0 = (int)(u / tiles_m) * 64;
+        float in[2][8];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {  // storage row n, elements m .. m+7
+            const int idx = t + 256 * i, row = idx >> 3, seg = idx & 7;
+            const int n = n0 + row, m = m0 + seg * 8;
+            const int cnt = n < p.N ? (p.M - m < 8 ? p.M - m : 8) : 0;
+            if (cnt > 0) {
+                load8<BF>(p.X + (long long)n * p.ldx + m, cnt, in[i]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) in[i][j] = 0.0f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int idx = t + 256 * i, row = idx >> 3, seg = idx & 7;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) tile[row][seg * 8 + j] = in[i][j];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {  // C row m, elements n .. n+7
+            const int idx = t + 256 * i, mrow = idx >> 3, seg = idx & 7;
+            const int m = m0 + mrow, n = n0 + seg * 8;
+            if (m >= p.M || n >= p.N) continue;
+            const int cnt = p.N - n < 8 ? p.N - n : 8;
+            float y[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) y[j] = tile[seg * 8 + j][mrow];
+            if (p.scale) {
+                const float s = f32_of<BF>(p.scale[m]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) y[j] *= s;
+            }
+            if (p.bias) {
+                float b[8];
+                load8<BF>(p.bias + n, cnt, b);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) y[j] += b[j];
+            }
+            if (p.relu) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) y[j] = fmaxf(y[j], 0.0f);
+            }
+            if (p.R) {
+                float r[8];
+                load8<BF>(p.R + (long long)m * p.ldr + n, cnt, r);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) y[j] += r[j];
+            }
+            store8<BF>(p.C + (long long)m * p.ldc + n, cnt, y);
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_pointwise(const PwParams& p, bool transposed, bool bf16, int sms,
@@ -173,7 +240,18 @@ cudaError_t launch_pointwise(const PwParams& p, bool transposed, bool bf16, int 
         blocks = ((long long)p.M * ((p.N + 7) / 8) + 255) / 256;
     }
     const unsigned grid = (unsigned)(blocks < cap ? blocks : cap);
-    if (transposed) {
+    auto rows16 = [](const void* base, long long ld) {
+        return base == nullptr ||
+               ((reinterpret_cast<uintptr_t>(base) & 15u) == 0 && (ld * 2) % 16 == 0);
+    };
+    const bool vec = rows16(p.X, p.ldx) && rows16(p.C, p.ldc) && rows16(p.R, p.ldr) &&
+                     rows16(p.bias, 8);
+    if (transposed && vec) {
+        if (bf16)
+            pointwise_transposed_vec_kernel<true><<<grid, 256, 0, stream>>>(p);
+        else
+            pointwise_transposed_vec_kernel<false><<<grid, 256, 0, stream>>>(p);
+    } else if (transposed) {
         if (bf16)
             pointwise_transposed_kernel<true><<<grid, 256, 0, stream>>>(p);
         else
