@@ -362,12 +362,35 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def pointwise_lines(tg, flush, stream, peaks, steps, warmup) -> dict:
+    """The two 8192 x 8192 fp16 pointwise programs: row-major X with
+    relu(scale_m*X + bias_n) + R, and X given permuted with relu(scale_m*X +
+    bias_n).  GB/s of algorithmic bytes against the measured copy bandwidth."""
+    import synthetic as S
+    out = {}
+    for key, permX in (("pointwise_fp16_8192x8192_scale_bias_relu_residual", 0),
+                       ("pointwise_fp16_8192x8192_permuted_input", 1)):
+        pp = S.pointwise_problem(8192, 8192, S.F16, 1020 + permX, permX=permX,
+                                 bias=True, scale=True, residual=permX == 0)
+        pp["relu"] = True
+        dpw = DevicePointwise(tg, pp)
+        ts = time_kernel(dpw.call, steps, warmup, flush, stream)
+        t = statistics.median(ts) * 1e-3
+        gbs = dpw.bytes() / t / 1e9
+        out[key] = {"gbs": gbs, "hbm_frac": gbs / float(peaks.get("hbm_gbs", 6800.0)),
+                    "ms_median": t * 1e3, "bytes": dpw.bytes()}
+        del dpw
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--pointwise-only", action="store_true",
+                    help="time only the two 8192 x 8192 pointwise programs (one JSON line)")
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the other workloads and the CPU baseline (for profiling)")
     ap.add_argument("--workload", default="fp16_4096", help="headline workload key")
@@ -399,6 +422,15 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     peaks, peak_src = load_peaks()
     specs = workload_specs()
+
+    if args.pointwise_only:
+        lines = pointwise_lines(tg, flush, stream, peaks, args.steps, args.warmup)
+        if rank == 0:
+            print(json.dumps({"metric": "pointwise GB/s (fp16, 8192 x 8192)", "unit": "GB/s",
+                              "steps": args.steps, "warmup": args.warmup,
+                              "peak_gbs": float(peaks.get("hbm_gbs", 6800.0)),
+                              "workloads": lines}), flush=True)
+        return
 
     # ---------------- headline: device-resident inputs
     hp = make_problem(specs[args.workload])
@@ -499,19 +531,7 @@ def main():
             del dp
         fused, plain = others["fp16_8192x8192x4096_fused"], others["fp16_8192x8192x4096_plain"]
         others["fused_over_plain_time"] = fused["ms_median"] / plain["ms_median"]
-        import synthetic as S
-        for key, permX in (("pointwise_fp16_8192x8192_scale_bias_relu_residual", 0),
-                           ("pointwise_fp16_8192x8192_permuted_input", 1)):
-            pp = S.pointwise_problem(8192, 8192, S.F16, 1020 + permX, permX=permX,
-                                     bias=True, scale=True, residual=permX == 0)
-            pp["relu"] = True
-            dpw = DevicePointwise(tg, pp)
-            ts = time_kernel(dpw.call, 10, 3, flush, stream)
-            t = statistics.median(ts) * 1e-3
-            gbs = dpw.bytes() / t / 1e9
-            others[key] = {"gbs": gbs, "hbm_frac": gbs / float(peaks.get("hbm_gbs", 6800.0)),
-                           "ms_median": t * 1e3, "bytes": dpw.bytes()}
-            del dpw
+        others.update(pointwise_lines(tg, flush, stream, peaks, 10, 3))
         line["workloads"] = others
         if rank == 0:
             tfl, rows, secs, cores = oracle_sample_tflops(hp, args.cpu_seconds)
