@@ -163,28 +163,37 @@ __global__ void __launch_bounds__(256) pointwise_transposed_kernel(const PwParam
 
 // The same with 16-byte accesses, when X's rows, C's rows, R's rows and bias
 // all start on 16-byte boundaries: each thread moves two 8-element vectors
-// of storage rows in, and writes two 8-element vectors of C rows out.
+// of storage rows in, and writes two 8-element vectors of C rows out.  The
+// next tile's loads are issued before the current tile's stores, so a load
+// phase and a store phase are always in flight together.
+template <bool BF>
+__device__ __forceinline__ void load_tile_vec(const PwParams& p, int m0, int n0, int t,
+                                              float (&in)[2][8]) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {  // storage row n, elements m .. m+7
+        const int idx = t + 256 * i, row = idx >> 3, seg = idx & 7;
+        const int n = n0 + row, m = m0 + seg * 8;
+        const int cnt = n < p.N ? (p.M - m < 8 ? p.M - m : 8) : 0;
+        if (cnt > 0) {
+            load8<BF>(p.X + (long long)n * p.ldx + m, cnt, in[i]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) in[i][j] = 0.0f;
+        }
+    }
+}
+
 template <bool BF>
 __global__ void __launch_bounds__(256) pointwise_transposed_vec_kernel(const PwParams p) {
     __shared__ float tile[64][65];  // [n - n0][m - m0]
     const int t = threadIdx.x;
     const int tiles_m = (p.M + 63) / 64, tiles_n = (p.N + 63) / 64;
     const long long tiles = (long long)tiles_m * tiles_n;
-    for (long long u = blockIdx.x; u < tiles; u += gridDim.x) {
+    float in[2][8];
+    long long u = blockIdx.x;
+    if (u < tiles) load_tile_vec<BF>(p, (int)(u % tiles_m) * 64, (int)(u / tiles_m) * 64, t, in);
+    for (; u < tiles; u += gridDim.x) {
         const int m0 = (int)(u % tiles_m) * 64, n0 = (int)(u / tiles_m) * 64;
-        float in[2][8];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {  // storage row n, elements m .. m+7
-            const int idx = t + 256 * i, row = idx >> 3, seg = idx & 7;
-            const int n = n0 + row, m = m0 + seg * 8;
-            const int cnt = n < p.N ? (p.M - m < 8 ? p.M - m : 8) : 0;
-            if (cnt > 0) {
-                load8<BF>(p.X + (long long)n * p.ldx + m, cnt, in[i]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) in[i][j] = 0.0f;
-            }
-        }
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int idx = t + 256 * i, row = idx >> 3, seg = idx & 7;
@@ -192,6 +201,9 @@ __global__ void __launch_bounds__(256) pointwise_transposed_vec_kernel(const PwP
             for (int j = 0; j < 8; ++j) tile[row][seg * 8 + j] = in[i][j];
         }
         __syncthreads();
+        const long long nxt = u + gridDim.x;  // its loads overlap this tile's stores
+        if (nxt < tiles)
+            load_tile_vec<BF>(p, (int)(nxt % tiles_m) * 64, (int)(nxt / tiles_m) * 64, t, in);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {  // C row m, elements n .. n+7
             const int idx = t + 256 * i, mrow = idx >> 3, seg = idx & 7;
