@@ -460,33 +460,37 @@ def main():
     props = torch.cuda.get_device_properties(local)
     theo = props.multi_processor_count * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 * 8192 / 1e12
 
-    # ---------------- end to end through the public API with host buffers
+    # ---------------- end to end through the public API with host buffers:
+    # tg_gemm_host copies A, B (and any epilogue operand) in from page-locked
+    # host memory and C back out, overlapped with the block GEMMs
     import numpy as np
     pin = lambda a: None if a is None else torch.from_numpy(
         np.ascontiguousarray(a).view(np.int16)).pin_memory()
     host_in = {k: pin(hp.get(k)) for k in ("A", "B", "bias", "scale", "R")}
-    dev_in = {k: (None if v is None else torch.empty_like(v, device="cuda"))
-              for k, v in host_in.items()}
     hC = torch.empty((M, N), dtype=torch.int16).pin_memory()
-    dC = torch.empty_like(prob.C)
-    e2e_epi = tg.make_epilogue(dev_in["bias"], dev_in["scale"], hp.get("relu", False),
-                               dev_in["R"], hp.get("ldr", 0) or 0)
+    e2e_epi = tg.make_epilogue(host_in["bias"], host_in["scale"], hp.get("relu", False),
+                               host_in["R"], hp.get("ldr", 0) or 0)
+    host_ws_bytes = tg.tg_gemm_host_workspace_size(M, N, K, hp["dtype"], hp["permA"], hp["permB"],
+                                                   e2e_epi)
+    host_ws = torch.zeros(host_ws_bytes, dtype=torch.uint8, device="cuda")
 
     def e2e_step(s):
-        with torch.cuda.stream(s):
-            for k, h in host_in.items():
-                if h is not None:
-                    dev_in[k].copy_(h, non_blocking=True)
-            tg.gemm_ws(M, N, K, dev_in["A"], hp["lda"], hp["permA"], dev_in["B"], hp["ldb"],
-                       hp["permB"], dC, N, hp["dtype"], e2e_epi, prob.ws, prob.ws_bytes, s)
-            hC.copy_(dC, non_blocking=True)
+        tg.gemm_host(M, N, K, host_in["A"], hp["lda"], hp["permA"], host_in["B"], hp["ldb"],
+                     hp["permB"], hC, N, hp["dtype"], e2e_epi, host_ws, host_ws_bytes, s)
 
     e2e_times = time_kernel(e2e_step, max(5, args.steps // 2), 3, flush, stream)
     e2e_ms = max_over_ranks(statistics.mean(e2e_times), world)
     h2d = sum(2 * v.numel() for v in host_in.values() if v is not None)
     d2h = 2 * hC.numel()
-    if not np.array_equal(hC.numpy(), prob.C.cpu().numpy()):
+    # the blocks may split K differently from the whole-matrix call: equal
+    # within the parity tolerance, not necessarily bit for bit
+    got = hC.numpy().view(np.uint16)
+    want = prob.C.cpu().numpy().view(np.uint16)
+    dec = (lambda b: b.view(np.float16).astype(np.float64)) if hp["dtype"] == 0 else \
+        (lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+    if not np.all(np.abs(dec(got) - dec(want)) <= 1e-2 * np.maximum(1.0, np.abs(dec(want)))):
         raise RuntimeError("end-to-end result differs from the device-resident run")
+    del host_ws
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -513,7 +517,8 @@ def main():
                      "theoretical_tflops": theo,
                      "frac_theoretical": achieved / theo},
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "api": "tg_gemm_host (pinned host A, B, C; copies overlapped with block GEMMs)"},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,

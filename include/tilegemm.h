@@ -176,6 +176,55 @@ int tg_gemm_workspace_size_ex(int64_t M, int64_t N, int64_t K, const void* A, in
                               const tg_epilogue* epi, size_t* bytes);
 
 /*
+ * tg_gemm with A, B, C and the epilogue operands in page-locked HOST memory
+ * (cudaHostAlloc / cudaHostRegister); the same computation, layouts, perms,
+ * epilogue order and rounding as tg_gemm.  Host strides are any ld >= the
+ * row width, pointers 2-byte aligned.
+ *
+ * The host<->device copies overlap the arithmetic: C is cut into blocks of
+ * whole 256-row output-tile rows (about four blocks; TG_HOST_BLOCK_ROWS, a
+ * multiple of 256, overrides).  An inbound copy stream brings B and bias,
+ * then each block's rows of A, scale and R, into dense device images inside
+ * `workspace`; each block's GEMM (tg_gemm_ws, one kernel) starts as soon as
+ * its rows have arrived, the blocks alternating between `stream` and a side
+ * stream so that two run side by side; an outbound copy stream returns each
+ * block of C while later blocks are still arriving.  Each block is an independent
+ * sub-GEMM over whole output tiles (ninetoothed.org "Named layouts",
+ * section "Contract": one program instance per output block).
+ *
+ * workspace: device memory of the current device, 256-byte aligned, at
+ *   least tg_gemm_host_workspace_size() bytes (two stream-K scratch areas,
+ *   one per compute stream, zeroed before first use as for tg_gemm_ws, then
+ *   dense images of B, bias, scale, A, R and C), inside one allocation;
+ *   calls sharing a workspace must not overlap on the GPU.
+ * Ordering: the copies start after the work already queued on `stream`, and
+ *   work queued on `stream` after the call starts once C is back in host
+ *   memory.  The call returns without synchronising; the two copy streams, the
+ *   side stream and their events are made once per device and reused (calls
+ *   from several host threads enqueue one at a time).
+ * Errors (all before any device work): as tg_gemm's shape, enum and stride
+ *   checks; TG_ERR_ALIGN for an odd host address or a workspace not 256-byte
+ *   aligned; TG_ERR_OVERLAP if C's bytes meet an input's or the workspace's;
+ *   TG_ERR_POINTER if a host span does not start and end in page-locked host
+ *   memory, or the workspace is not device memory of the current device
+ *   covering the bytes needed; TG_ERR_BUFFER if workspace_bytes is too small.
+ *   TG_ERR_CUDA if a copy or launch fails while enqueuing (work already
+ *   queued then still runs, and `stream` still waits for it).
+ */
+int tg_gemm_host(int64_t M, int64_t N, int64_t K,
+                 const void* A, int64_t lda, tg_perm permA,
+                 const void* B, int64_t ldb, tg_perm permB,
+                 void* C, int64_t ldc, tg_dtype dtype,
+                 const tg_epilogue* epi, void* workspace, size_t workspace_bytes,
+                 cudaStream_t stream);
+
+/* Workspace bytes tg_gemm_host needs for this shape on the current device
+ * (independent of the host strides; `epi` only says which epilogue operands
+ * are present).  Errors as tg_gemm's shape and enum checks. */
+int tg_gemm_host_workspace_size(int64_t M, int64_t N, int64_t K, tg_perm permA, tg_perm permB,
+                                tg_dtype dtype, const tg_epilogue* epi, size_t* bytes);
+
+/*
  * Pointwise program of the named-layout pages (ninetoothed.org "Named
  * layouts": pointwise work, missing-axis broadcasting, reordering and
  * same-output-domain bias/ReLU/residual postprocessing):

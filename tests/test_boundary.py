@@ -143,3 +143,25 @@ def test_workspace_call_accepts_unaligned_operands_before_the_device_check(tg):
     rc = tg.tg_gemm(256, 256, 250, FAKE + 2, 250, N_, FAKE + (1 << 30), 256, N_,
                     FAKE + (2 << 30) + 6, 257, F16, None)
     assert rc == tg.TG_ERR_ALIGN
+
+
+def test_host_pipeline_checks_shape_before_the_device(tg):
+    # tg_gemm_host: sizes, null pointers, enums and dtype are refused before
+    # any device query; valid arguments reach the device check
+    A, B, C, W = FAKE, FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (3 << 30)
+    host = lambda M=256, N=256, K=256, pa=0, pb=0, dt=F16, w=W, epi=None: tg.tg_gemm_host(
+        M, N, K, A, K, pa, B, N, pb, C, N, dt, epi, w, 1 << 30)
+    assert host(M=0) == tg.TG_ERR_INVALID_ARG
+    assert host(K=1 << 31) == tg.TG_ERR_INVALID_ARG
+    assert host(w=None) == tg.TG_ERR_INVALID_ARG
+    assert host(pa=2) == tg.TG_ERR_INVALID_ARG
+    assert host(dt=7) == tg.TG_ERR_DTYPE
+    assert host(epi=tg.make_epilogue(relu=3)) == tg.TG_ERR_INVALID_ARG
+    assert host() == tg.TG_ERR_UNSUPPORTED_DEVICE
+    n = ctypes.c_size_t(0)
+    assert tg._lib.tg_gemm_host_workspace_size(256, 256, 256, 0, 0, F16, None, None) == \
+        tg.TG_ERR_INVALID_ARG
+    assert tg._lib.tg_gemm_host_workspace_size(0, 256, 256, 0, 0, F16, None, ctypes.byref(n)) == \
+        tg.TG_ERR_INVALID_ARG
+    assert tg._lib.tg_gemm_host_workspace_size(256, 256, 256, 0, 0, F16, None, ctypes.byref(n)) == \
+        tg.TG_ERR_UNSUPPORTED_DEVICE

@@ -75,6 +75,10 @@ _sig("tg_gemm_workspace_size_ex", _int, _i64, _i64, _i64, _vp, _i64, _int, _vp, 
      _i64, _int, ctypes.POINTER(tg_epilogue), ctypes.POINTER(ctypes.c_size_t))
 _sig("tg_gemm_static_ws", _int, _i64, _i64, _i64, _vp, _i64, _int, _vp, _i64, _int, _vp, _i64,
      _int, ctypes.POINTER(tg_epilogue), _vp)
+_sig("tg_gemm_host", _int, _i64, _i64, _i64, _vp, _i64, _int, _vp, _i64, _int, _vp, _i64, _int,
+     ctypes.POINTER(tg_epilogue), _vp, ctypes.c_size_t, _vp)
+_sig("tg_gemm_host_workspace_size", _int, _i64, _i64, _i64, _int, _int, _int,
+     ctypes.POINTER(tg_epilogue), ctypes.POINTER(ctypes.c_size_t))
 _sig("tg_debug_status", _int, ctypes.POINTER(_int))
 _sig("tg_debug_configure", _int, _i64, _i64)
 _sig("tg_probe_swizzle128", _int, _vp, _int, _i64, _vp, _vp, _vp)
@@ -112,7 +116,7 @@ _sig("tg_layout_tmem_32x32b", _int, _int, _PP)
 EXPORTED = [
     "tg_gemm", "tg_gemm_ws", "tg_gemm_workspace_size", "tg_gemm_workspace_size_ex",
     "tg_pointwise",
-    "tg_gemm_static_ws",
+    "tg_gemm_static_ws", "tg_gemm_host", "tg_gemm_host_workspace_size",
     "tg_status_string", "tg_query_config",
     "tg_query_config_ws", "tg_query_config_for_sms",
     "tg_debug_status", "tg_debug_configure",
@@ -206,6 +210,33 @@ def tg_gemm_workspace_size(M, N, K, dtype, permA=TG_OP_N, permB=TG_OP_N, epi=Non
                                      ctypes.byref(n))
     if rc != TG_OK:
         raise TileGemmError(rc, "tg_gemm_workspace_size")
+    return n.value
+
+
+def tg_gemm_host(M, N, K, A, lda, permA, B, ldb, permB, C, ldc, dtype, epi, workspace,
+                 workspace_bytes, stream=None) -> int:
+    """Status of one tg_gemm_host call (A, B, C and the epilogue operands in
+    page-locked host memory, `workspace` on the device); never raises."""
+    return _lib.tg_gemm_host(M, N, K, _addr(A), lda, permA, _addr(B), ldb, permB, _addr(C), ldc,
+                             dtype, ctypes.byref(epi) if epi is not None else None,
+                             _addr(workspace), workspace_bytes, _stream(stream))
+
+
+def gemm_host(M, N, K, A, lda, permA, B, ldb, permB, C, ldc, dtype, epi, workspace,
+              workspace_bytes, stream=None) -> None:
+    rc = tg_gemm_host(M, N, K, A, lda, permA, B, ldb, permB, C, ldc, dtype, epi, workspace,
+                      workspace_bytes, stream)
+    if rc != TG_OK:
+        raise TileGemmError(rc, "tg_gemm_host")
+
+
+def tg_gemm_host_workspace_size(M, N, K, dtype, permA=TG_OP_N, permB=TG_OP_N, epi=None) -> int:
+    n = ctypes.c_size_t(0)
+    rc = _lib.tg_gemm_host_workspace_size(M, N, K, permA, permB, dtype,
+                                          ctypes.byref(epi) if epi is not None else None,
+                                          ctypes.byref(n))
+    if rc != TG_OK:
+        raise TileGemmError(rc, "tg_gemm_host_workspace_size")
     return n.value
 
 

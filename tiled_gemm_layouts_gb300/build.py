@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtilegemm.so")
 
 CUDA_SOURCES = ["api.cu", "gemm_sm103.cu", "probes.cu", "noalloc.cu", "stage.cu", "pointwise.cu"] + [f"gemm_inst_{i}.cu" for i in range(1, 37)]
-CXX_SOURCES = ["layout.cpp", "select.cpp"]
+CXX_SOURCES = ["layout.cpp", "select.cpp", "host_pipeline.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
