@@ -160,14 +160,33 @@ __device__ __forceinline__ uint32_t pack2t(float a, float b) {
     return w;
 }
 
+// y[0], y[1] += x0, x1 as one packed fp32x2 add (round to nearest): half
+// the arithmetic instructions of the epilogue warps, which share issue slots
+// with the single-thread producer and MMA loops.
+__device__ __forceinline__ void add2(float* y, float x0, float x1) {
+    unsigned long long a, b;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(y[0]), "f"(y[1]));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(x0), "f"(x1));
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(b));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(y[0]), "=f"(y[1]) : "l"(a));
+}
+
+// y[0], y[1] *= s as one packed fp32x2 multiply (round to nearest).
+__device__ __forceinline__ void mul2(float* y, float s) {
+    unsigned long long a, b;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(y[0]), "f"(y[1]));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(b) : "f"(s));
+    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(b));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(y[0]), "=f"(y[1]) : "l"(a));
+}
+
 template <bool BF>
 __device__ __forceinline__ void add8(const uint4& u, float* y) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float2 f = unpack2<BF>(w[i]);
-        y[2 * i] += f.x;
-        y[2 * i + 1] += f.y;
+        add2(y + 2 * i, f.x, f.y);
     }
 }
 
@@ -207,7 +226,7 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int m, int c0
     const bool full = inside && c0 + 32 <= p.N;
     if (p.scale_m) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) y[j] *= row_scale;
+        for (int j = 0; j < 32; j += 2) mul2(y + j, row_scale);
     }
     if (p.bias_n && inside) {
         const uint16_t* b = static_cast<const uint16_t*>(p.bias_n) + c0;
