@@ -19,6 +19,11 @@ def test_benchmark_workload_choices(tg):
     assert (c["swap"], c["pair"], c["bm"], c["bn"], c["grid"]) == (0, 1, 256, 256, 152)
     c = cfg(tg, 8192, 8192, 4096, F16, 0, 0)
     assert (c["pair"], c["bn"], c["tiles"]) == (1, 256, 1024)
+    # K = 1000 (16 K-blocks) is too shallow for stream-K: both 256 x 256 (192
+    # tiles) and 256 x 224 (224 tiles) take three whole waves and stage 256
+    # B columns per tile; the narrower one computes fewer columns
+    c = cfg(tg, 4000, 3000, 1000, F16, 1, 0)
+    assert (c["pair"], c["bm"], c["bn"], c["tiles"], c["sk_tiles"]) == (1, 256, 224, 224, 0)
     # M = 32 cannot fill the accumulator lanes: operands swap, one 32-wide column
     c = cfg(tg, 32, 16384, 16384, BF16, 0, 0)
     assert (c["swap"], c["pair"], c["bn"], c["tiles"], c["grid"]) == (1, 0, 32, 128, 128)

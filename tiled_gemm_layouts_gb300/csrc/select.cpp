@@ -105,6 +105,10 @@ KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int p
          forced_sk = false;
     apply_override(c, forced_bn, forced_pair, forced_swap, forced_no_sk, forced_sk);
 
+    // Stream-K only deals out tails of tiles at least 32 K-blocks deep (see
+    // below), so only then may the wave estimate count on it.
+    const bool sk_possible = allow_sk && (K + 63) / 64 >= 32;
+    const bool shallow = (K + 63) / 64 < 32;
     Choice best{0, 0, 0, -1.0};
     for (int swap = 0; swap < 2; ++swap) {
         if (forced_swap && swap != c.swap) continue;
@@ -121,7 +125,7 @@ KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int p
                 const int bm = pair ? 256 : 128;
                 const int slots = pair ? sms / 2 : sms;
                 const int64_t tiles = cdiv(Mk, bm) * cdiv(Nk, bn);
-                const double waves = effective_waves(tiles, slots, allow_sk);
+                const double waves = effective_waves(tiles, slots, sk_possible);
                 const int cols = staged_columns(bn, pair, q_mn);
                 double score = (double)Mk * (double)Nk / (waves * slots * bm * cols) *
                                tile_efficiency(cols, pair);
@@ -133,7 +137,15 @@ KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int p
                 // per lane and measured 12% slower at 4096^3.
                 const bool small_m = M <= 64 && N > M;
                 if (swap != (small_m ? 1 : 0) && !forced_swap) continue;
-                if (score > best.score + 1e-9) best = Choice{swap, pair, bn, score};
+                // Equal modelled cost (same waves, same staged columns) with
+                // a shallow K, where the ring hides most loads and tensor
+                // work sets a tile's time: the narrower tile computes fewer
+                // columns (4000 x 3000 x 1000, B row-major: 256 x 224
+                // measured 5 % faster than 256 x 256, both three whole
+                // waves).  Deep tiles are load-bound: keep the wider one.
+                if (score > best.score + 1e-9 ||
+                    (shallow && score > best.score - 1e-9 && pair == best.pair && bn < best.bn))
+                    best = Choice{swap, pair, bn, score};
             }
         }
     }
