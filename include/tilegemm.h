@@ -394,6 +394,18 @@ int tg_layout_blocked(const int size_per_thread[2], const int threads_per_warp[2
                       const int warps_per_cta[2], const int order[2], const int shape[2],
                       tg_layout** out);
 
+/* The same rule for a tensor of any rank 1..8: (register, lane, warp) ->
+ * (dim0, ..., dim{rank-1}); each array has `rank` entries and `order` is a
+ * permutation of 0..rank-1 (minor dim first).  Lane and warp ids split over
+ * the dims in `order`; registers hold first the per-thread elements, then the
+ * CTA tile's repetitions (section "Blocked-layout example", the encoding
+ * the rank-2 example instantiates).  TG_ERR_INVALID_ARG for a null pointer or
+ * rank outside 1..8, TG_ERR_LAYOUT for a size that is not a power of two, an
+ * order that is not a permutation, or more bits than the module holds. */
+int tg_layout_blocked_nd(int rank, const int* size_per_thread, const int* threads_per_warp,
+                         const int* warps_per_cta, const int* order, const int* shape,
+                         tg_layout** out);
+
 /* Cooperative traversal of a rank-2 tile by `threads` threads
  * (pbelevich.github.io Part 12, "Cooperative tile layouts": thread t at
  * iteration i visits linear index t + i*threads, peeled axis by axis in

@@ -55,6 +55,42 @@ def test_blocked_constructor_matches_integer_rule(tg, spt, tpw, wpc, order, shap
                                                   x["lane"], x["warp"]))
 
 
+@pytest.mark.parametrize("spt,tpw,wpc,order,shape", [
+    ([1], [32], [4], [0], [512]),                                      # rank 1, repetitions
+    ([1, 1, 1], [1, 1, 32], [1, 4, 1], [2, 1, 0], [1, 32, 32]),        # a unit dim before 2-D
+    ([2, 1, 4], [2, 4, 4], [1, 2, 2], [2, 0, 1], [8, 16, 64]),
+    ([1, 2, 2], [4, 2, 4], [2, 2, 1], [0, 2, 1], [4, 32, 16]),         # dim0 tile wider: broadcast
+    ([1, 1, 2, 2], [2, 2, 2, 4], [1, 2, 1, 2], [3, 2, 1, 0], [4, 8, 8, 32]),
+])
+def test_blocked_nd_matches_integer_rule(tg, spt, tpw, wpc, order, shape):
+    L = tg.LinearLayout.blocked_nd(spt, tpw, wpc, order, shape)
+    assert L.out_dims == [(f"dim{d}", int(np.log2(shape[d]))) for d in range(len(shape))]
+    same_table(L, lambda x: lo.blocked_coordinate(spt, tpw, wpc, order, shape, x["register"],
+                                                  x["lane"], x["warp"]))
+
+
+def test_blocked_nd_rank2_is_the_rank2_constructor(tg):
+    args = ([2, 4], [4, 8], [2, 2], [1, 0], [64, 128])
+    assert tg.LinearLayout.blocked_nd(*args).bases == tg.LinearLayout.blocked(*args).bases
+
+
+def test_blocked_nd_checks(tg):
+    bad = [
+        ([1, 1, 1], [1, 1, 32], [1, 4, 1], [2, 2, 0], [1, 32, 32]),   # order not a permutation
+        ([1, 1, 1], [1, 1, 32], [1, 4, 1], [2, 1, 3], [1, 32, 32]),   # order out of range
+        ([1, 1, 1], [1, 1, 24], [1, 4, 1], [2, 1, 0], [1, 32, 32]),   # not a power of two
+    ]
+    for args in bad:
+        with pytest.raises(tg.TileGemmError) as e:
+            tg.LinearLayout.blocked_nd(*args)
+        assert e.value.status == tg.TG_ERR_LAYOUT
+    with pytest.raises(tg.TileGemmError) as e:
+        tg.LinearLayout.blocked_nd([1] * 9, [1] * 9, [1] * 9, list(range(9)), [2] * 9)
+    assert e.value.status == tg.TG_ERR_INVALID_ARG
+    with pytest.raises(tg.TileGemmError):
+        tg.LinearLayout.blocked_nd([1, 1], [1], [1, 1], [1, 0], [2, 2])  # ragged arguments
+
+
 @pytest.mark.parametrize("shape,threads,order", [
     ((4, 16), 32, (1, 0)), ((16, 8), 32, (1, 0)), ((64, 64), 256, (1, 0)),
     ((8, 32), 64, (0, 1)), ((32, 32), 32, (1, 0)),

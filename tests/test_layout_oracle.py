@@ -151,3 +151,48 @@ def test_tmem_32x32b_definition():
     assert lo.tmem_32x32b_coordinate(2, 5, 7, 32) == (69, 39)
     rows = {lo.tmem_32x32b_coordinate(w, t, 0)[0] for w in range(4) for t in range(32)}
     assert rows == set(range(128))
+
+
+def test_blocked_rank3_with_a_unit_dim_reproduces_the_printed_example():
+    # the rank-generic owner rule, pinned to the page's rank-2 example: a
+    # leading dim of size 1 changes no coordinate of the other two
+    g = load_golden("blocked_32x32.json")
+    spt, tpw, wpc, order, shape = (g["size_per_thread"], g["threads_per_warp"],
+                                   g["warps_per_cta"], g["order"], g["shape"])
+    for r in range(8):
+        for l in range(32):
+            for w in range(4):
+                c2 = lo.blocked_coordinate(spt, tpw, wpc, order, shape, r, l, w)
+                c3 = lo.blocked_coordinate([1] + spt, [1] + tpw, [1] + wpc,
+                                           [o + 1 for o in order] + [0], [1] + shape, r, l, w)
+                assert c3 == (0,) + c2
+
+
+@pytest.mark.parametrize("spt,tpw,wpc,order", [
+    ([2, 1, 4], [2, 4, 4], [1, 2, 2], [2, 0, 1]),
+    ([1, 2, 1, 2], [2, 2, 4, 2], [2, 1, 2, 1], [1, 3, 0, 2]),
+])
+def test_blocked_rank_n_is_a_bijection_on_one_cta_tile(spt, tpw, wpc, order):
+    # shape == CTA tile: every element has exactly one owner
+    shape = [s * t * w for s, t, w in zip(spt, tpw, wpc)]
+    regs = int(np.prod(spt))
+    lanes, warps = int(np.prod(tpw)), int(np.prod(wpc))
+    seen = {lo.blocked_coordinate(spt, tpw, wpc, order, shape, r, l, w)
+            for r in range(regs) for l in range(lanes) for w in range(warps)}
+    assert len(seen) == int(np.prod(shape)) == regs * lanes * warps
+    assert all(all(0 <= c[d] < shape[d] for d in range(len(shape))) for c in seen)
+
+
+def test_blocked_rank_n_permuting_dims_permutes_coordinates():
+    # relabelling dims (order relabelled to match) relabels each coordinate
+    spt, tpw, wpc, order, shape = [2, 1, 4], [2, 4, 4], [1, 2, 2], [2, 0, 1], [8, 16, 64]
+    perm = [1, 2, 0]  # new dim i is old dim perm[i]
+    inv = [perm.index(d) for d in range(3)]
+    P = lambda v: [v[perm[i]] for i in range(3)]
+    for r in range(16):
+        for l in range(32):
+            for w in range(4):
+                a = lo.blocked_coordinate(spt, tpw, wpc, order, shape, r, l, w)
+                b = lo.blocked_coordinate(P(spt), P(tpw), P(wpc), [inv[d] for d in order],
+                                          P(shape), r, l, w)
+                assert b == tuple(P(a))

@@ -108,6 +108,8 @@ _sig("tg_layout_is_surjective", _int, _vp, ctypes.POINTER(_int))
 _sig("tg_layout_invert_and_compose", _int, _vp, _vp, _PP)
 _I2 = ctypes.c_int * 2
 _sig("tg_layout_blocked", _int, _I2, _I2, _I2, _I2, _I2, _PP)
+_IP = ctypes.POINTER(_int)
+_sig("tg_layout_blocked_nd", _int, _int, _IP, _IP, _IP, _IP, _IP, _PP)
 _sig("tg_layout_cooperative", _int, _I2, _int, _I2, _PP)
 _sig("tg_layout_register_tile", _int, _I2, _I2, _PP)
 _sig("tg_layout_swizzle128", _int, _int, _int, _PP)
@@ -127,6 +129,7 @@ EXPORTED = [
     "tg_layout_reshape_outs", "tg_layout_divide_left", "tg_layout_divide_right",
     "tg_layout_rank", "tg_layout_is_injective",
     "tg_layout_is_surjective", "tg_layout_invert_and_compose", "tg_layout_blocked",
+    "tg_layout_blocked_nd",
     "tg_layout_cooperative", "tg_layout_register_tile", "tg_layout_swizzle128",
     "tg_layout_tmem_32x32b",
 ]
@@ -462,6 +465,16 @@ class LinearLayout:
     def blocked(cls, size_per_thread, threads_per_warp, warps_per_cta, order, shape):
         return cls._new(_lib.tg_layout_blocked, _I2(*size_per_thread), _I2(*threads_per_warp),
                         _I2(*warps_per_cta), _I2(*order), _I2(*shape), what="blocked")
+
+    @classmethod
+    def blocked_nd(cls, size_per_thread, threads_per_warp, warps_per_cta, order, shape):
+        """Blocked encoding of any rank (every argument has one entry per dim)."""
+        rank = len(shape)
+        if any(len(x) != rank for x in (size_per_thread, threads_per_warp, warps_per_cta, order)):
+            raise TileGemmError(TG_ERR_INVALID_ARG, "blocked_nd")
+        arrs = [(_int * rank)(*x) for x in (size_per_thread, threads_per_warp, warps_per_cta,
+                                             order, shape)]
+        return cls._new(_lib.tg_layout_blocked_nd, rank, *arrs, what="blocked_nd")
 
     @classmethod
     def cooperative(cls, shape, threads, order):

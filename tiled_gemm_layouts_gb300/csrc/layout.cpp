@@ -591,16 +591,19 @@ int tg_layout_invert_and_compose(const tg_layout* R, const tg_layout* S, tg_layo
     });
 }
 
-int tg_layout_blocked(const int size_per_thread[2], const int threads_per_warp[2],
-                      const int warps_per_cta[2], const int order[2], const int shape[2],
-                      tg_layout** out) {
-    if (!size_per_thread || !threads_per_warp || !warps_per_cta || !order || !shape || !out)
+int tg_layout_blocked_nd(int rank, const int* size_per_thread, const int* threads_per_warp,
+                         const int* warps_per_cta, const int* order, const int* shape,
+                         tg_layout** out) {
+    if (!size_per_thread || !threads_per_warp || !warps_per_cta || !order || !shape || !out ||
+        rank < 1 || rank > 8)
         return TG_ERR_INVALID_ARG;
     return guarded([&] {
-        if (!((order[0] == 0 && order[1] == 1) || (order[0] == 1 && order[1] == 0)))
-            throw LayoutError();
-        int lg_spt[2], lg_tpw[2], lg_wpc[2], lg_shape[2], lg_rep[2];
-        for (int d = 0; d < 2; ++d) {
+        std::vector<int> seen(rank, 0);  // `order` is a permutation of 0 .. rank-1
+        for (int k = 0; k < rank; ++k) {
+            if (order[k] < 0 || order[k] >= rank || seen[order[k]]++) throw LayoutError();
+        }
+        std::vector<int> lg_spt(rank), lg_tpw(rank), lg_wpc(rank), lg_shape(rank), lg_rep(rank);
+        for (int d = 0; d < rank; ++d) {
             lg_spt[d] = log2_exact(size_per_thread[d]);
             lg_tpw[d] = log2_exact(threads_per_warp[d]);
             lg_wpc[d] = log2_exact(warps_per_cta[d]);
@@ -611,29 +614,28 @@ int tg_layout_blocked(const int size_per_thread[2], const int threads_per_warp[2
         // Coordinate (1 << lg) along dim d, or a broadcast (zero) basis when
         // the CTA tile is larger than the tensor along d.
         auto basis = [&](int d, int lg) {
-            std::vector<int32_t> v(2, 0);
+            std::vector<int32_t> v(rank, 0);
             if (lg < lg_shape[d]) v[d] = 1 << lg;
             return v;
         };
-        int nreg = 0, nlane = 0, nwarp = 0;
-        tg_layout* l = make({"register", "lane", "warp"}, {0, 0, 0}, {"dim0", "dim1"},
-                            {lg_shape[0], lg_shape[1]});
+        std::vector<std::string> out_names;
+        for (int d = 0; d < rank; ++d) out_names.push_back("dim" + std::to_string(d));
+        tg_layout* l = make({"register", "lane", "warp"}, {0, 0, 0}, out_names, lg_shape);
+        // per dim in `order` (minor first): the thread's own elements, then
+        // lanes, then warps; then the CTA tile's repetitions as more registers
         std::vector<std::vector<int32_t>> reg, lane, warp;
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < rank; ++k) {
             const int d = order[k];
             for (int i = 0; i < lg_spt[d]; ++i) reg.push_back(basis(d, i));
             for (int i = 0; i < lg_tpw[d]; ++i) lane.push_back(basis(d, lg_spt[d] + i));
             for (int i = 0; i < lg_wpc[d]; ++i) warp.push_back(basis(d, lg_spt[d] + lg_tpw[d] + i));
         }
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < rank; ++k) {
             const int d = order[k];
             for (int i = 0; i < lg_rep[d]; ++i)
                 reg.push_back(basis(d, lg_spt[d] + lg_tpw[d] + lg_wpc[d] + i));
         }
-        nreg = (int)reg.size();
-        nlane = (int)lane.size();
-        nwarp = (int)warp.size();
-        l->in_bits = {nreg, nlane, nwarp};
+        l->in_bits = {(int)reg.size(), (int)lane.size(), (int)warp.size()};
         for (auto* group : {&reg, &lane, &warp})
             for (auto& v : *group) l->bases.push_back(v);
         try {
@@ -645,6 +647,13 @@ int tg_layout_blocked(const int size_per_thread[2], const int threads_per_warp[2
         *out = l;
         return TG_OK;
     });
+}
+
+int tg_layout_blocked(const int size_per_thread[2], const int threads_per_warp[2],
+                      const int warps_per_cta[2], const int order[2], const int shape[2],
+                      tg_layout** out) {
+    return tg_layout_blocked_nd(2, size_per_thread, threads_per_warp, warps_per_cta, order, shape,
+                                out);
 }
 
 int tg_layout_cooperative(const int shape[2], int threads, const int order[2], tg_layout** out) {
