@@ -20,6 +20,8 @@
 
 #include <cuda_runtime_api.h> /* cudaStream_t */
 
+#include "tilegemm_layout_device.h" /* tg_folded_layout */
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -405,6 +407,24 @@ int tg_layout_blocked(const int size_per_thread[2], const int threads_per_warp[2
 int tg_layout_blocked_nd(int rank, const int* size_per_thread, const int* threads_per_warp,
                          const int* warps_per_cta, const int* order, const int* shape,
                          tg_layout** out);
+
+/* Folds a layout for evaluation in a kernel (retepy.com "Triton
+ * LinearLayout", section "applyLinearLayout"): the inputs named in
+ * fixed_names take fixed_values and are applied once, giving the constant
+ * part of every output; every other input dim stays variable, in the
+ * layout's input order, and contributes one packed column per bit.  Evaluate
+ * with tg_folded_apply_packed / tg_folded_output (tilegemm_layout_device.h,
+ * host or device).  `out` is plain data owned by the caller.
+ * TG_ERR_INVALID_ARG for null pointers or n_fixed < 0; TG_ERR_LAYOUT for an
+ * unknown or repeated name, a value outside its dim, more than 8 variable
+ * dims or 32 variable bits, or more than 8 output dims or 32 output bits. */
+int tg_layout_fold(const tg_layout* l, int n_fixed, const char* const* fixed_names,
+                   const int32_t* fixed_values, tg_folded_layout* out);
+
+/* Host evaluation of a folded layout through the same inline functions a
+ * kernel uses: outs[o] for variable inputs vars[0 .. n_vars).
+ * TG_ERR_INVALID_ARG for a null pointer or a value outside its dim. */
+int tg_layout_folded_apply(const tg_folded_layout* f, const int32_t* vars, int32_t* outs);
 
 /* Cooperative traversal of a rank-2 tile by `threads` threads
  * (pbelevich.github.io Part 12, "Cooperative tile layouts": thread t at

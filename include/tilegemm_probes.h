@@ -21,6 +21,8 @@
 
 #include <cuda_runtime_api.h>
 
+#include "tilegemm_layout_device.h" /* tg_folded_layout */
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -38,6 +40,15 @@ int tg_probe_swizzle128(const void* src, int rows, int64_t ld, void* dst, int* s
  * warp `warp` received in that register.  bn: 64, 128 or 256; dst holds
  * 128*bn uint32. */
 int tg_probe_tmem_32x32b(int bn, void* dst, int* status_dev, cudaStream_t stream);
+
+/* Device evaluation of a folded layout (tg_layout_fold): thread c splits c
+ * into the variable inputs (first variable dim in the lowest bits), applies
+ * the layout with tg_folded_apply_packed and writes output o to
+ * dst[c*n_outs + o] (int32).  f->n_bits <= 20; dst: device memory of the
+ * current device, at least 2^n_bits * n_outs * 4 bytes (TG_ERR_BUFFER
+ * otherwise, TG_ERR_POINTER if dst is not device memory). */
+int tg_probe_folded_layout(const tg_folded_layout* f, void* dst, size_t dst_bytes,
+                           cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -20,7 +20,9 @@ def declared_symbols():
         if h.endswith(".h"):
             src = open(os.path.join(ROOT, "include", h)).read()
             src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-            names |= set(re.findall(r"\b(tg_\w+)\s*\(", src))
+            # header-only inline helpers (for kernels) are not library symbols
+            inline = set(re.findall(r"TG_LAYOUT_FN\s+\w+\s+(tg_\w+)\s*\(", src))
+            names |= set(re.findall(r"\b(tg_\w+)\s*\(", src)) - inline
     return names
 
 

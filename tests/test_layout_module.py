@@ -394,3 +394,69 @@ def test_divide_rejects_a_non_factor(tg):
     big = tg.LinearLayout.create([("lane", 3)], [("x", 1)], {"lane": [(1,), (0,), (0,)]})
     with pytest.raises(tg.TileGemmError):  # B needs more output bits than A has left
         tg.LinearLayout.create([("lane", 1)], [("x", 1)], {"lane": [(1,)]}).divide_left(big)
+
+
+def folded_cases(tg):
+    g = load_golden("linear_layout_lane_warp.json")
+    page = tg.LinearLayout.create([tuple(d) for d in g["in_dims"]],
+                                  [tuple(d) for d in g["out_dims"]], g["bases"])
+    blocked = tg.LinearLayout.blocked([2, 4], [4, 8], [2, 2], [1, 0], [64, 128])
+    tmem = tg.LinearLayout.tmem_32x32b(256)
+    swz = tg.LinearLayout.swizzle128(64, 2)
+    nd = tg.LinearLayout.blocked_nd([1, 2, 2], [4, 2, 4], [2, 2, 1], [0, 2, 1], [4, 32, 16])
+    return [
+        (page, {}), (page, {"warp": 2}), (page, {"lane": 3, "warp": 1}),
+        # the page's example: register 3 folded, lane and warp variable
+        (blocked, {"register": 3}), (blocked, {"warp": 2}), (blocked, {}),
+        (tmem, {"register": 17}), (tmem, {"warp": 3, "lane": 5}),
+        (swz, {}), (nd, {"register": 5, "warp": 1}),
+    ]
+
+
+def test_folded_layout_matches_apply_on_every_input(tg):
+    for L, fixed in folded_cases(tg):
+        F = L.fold(fixed)
+        T = tuple_of(L)
+        for x in lo.all_inputs(T):
+            if any(x[n] != v for n, v in fixed.items()):
+                continue
+            want = lo.apply(T, x)
+            assert F.apply({n: x[n] for n in F.var_names}) == want, (fixed, x)
+            assert L.apply(x) == want
+
+
+def test_folded_layout_structure(tg):
+    # constant part = the layout applied to the fixed inputs alone; one packed
+    # column per variable bit; outputs packed low to high in layout order
+    L = tg.LinearLayout.blocked([2, 4], [4, 8], [2, 2], [1, 0], [64, 128])
+    F = L.fold({"register": 3})
+    r = F.raw
+    assert r.n_vars == 2 and list(r.var_bits[:2]) == [5, 2] and r.n_bits == 7
+    assert r.n_outs == 2 and list(r.out_shift[:2]) == [0, 6] and list(r.out_bits[:2]) == [6, 7]
+    c = L.apply({"register": 3, "lane": 0, "warp": 0})
+    assert r.constant == c[0] | (c[1] << 6)
+    lane_bases = L.bases["lane"]
+    for i, (d0, d1) in enumerate(lane_bases):
+        assert r.cols[i] == d0 | (d1 << 6)
+
+
+def test_fold_checks(tg):
+    L = tg.LinearLayout.blocked([2, 4], [4, 8], [2, 2], [1, 0], [64, 128])
+    for fixed in ({"nope": 0}, {"lane": 32}, {"lane": -1}):
+        with pytest.raises(tg.TileGemmError) as e:
+            L.fold(fixed)
+        assert e.value.status == tg.TG_ERR_LAYOUT
+    F = L.fold({})
+    with pytest.raises(tg.TileGemmError) as e:
+        F.apply({"register": 64, "lane": 0, "warp": 0})  # register has 5 bits
+    assert e.value.status == tg.TG_ERR_INVALID_ARG
+    # more than 32 variable input bits cannot be packed into one word
+    big = tg.LinearLayout.create([("a", 20), ("b", 20)], [("x", 20), ("y", 20)],
+                                 {"a": [(1 << i, 0) for i in range(20)],
+                                  "b": [(0, 1 << i) for i in range(20)]})
+    with pytest.raises(tg.TileGemmError) as e:
+        big.fold({})
+    assert e.value.status == tg.TG_ERR_LAYOUT
+    with pytest.raises(tg.TileGemmError) as e:
+        big.fold({"a": 5})  # 20 variable bits fit, but the outputs need 40
+    assert e.value.status == tg.TG_ERR_LAYOUT

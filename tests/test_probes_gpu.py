@@ -3,8 +3,13 @@
 * the 128-byte swizzle a TMA copy writes into shared memory equals the
   (offset) -> (row, col) layout ``swizzle128`` and the oracle's definition;
 * the accumulator readout of tcgen05.ld 32x32b equals the
-  (register, lane, warp) -> (m, n) layout ``tmem_32x32b``.
+  (register, lane, warp) -> (m, n) layout ``tmem_32x32b``;
+* a layout folded for kernels (tilegemm_layout_device.h) evaluates on the
+  device to what the host module and the oracle give, for every variable
+  input.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -52,3 +57,29 @@ def test_tmem_readout_matches_layout(tg, bn):
                 assert v == 256 * m + n
                 assert (m, n) == L.apply({"register": j, "lane": t, "warp": w})
                 assert (m, n) == lo.tmem_32x32b_coordinate(w, t, j)
+
+
+def test_folded_layout_on_the_device(tg):
+    import torch
+    from test_layout_module import folded_cases
+    for L, fixed in folded_cases(tg):
+        F = L.fold(fixed)
+        r = F.raw
+        n = 1 << r.n_bits
+        dst = torch.full((n * r.n_outs,), -1, dtype=torch.int32, device="cuda")
+        assert tg._lib.tg_probe_folded_layout(ctypes.byref(r), dst.data_ptr(), dst.numel() * 4,
+                                              None) == tg.TG_OK
+        torch.cuda.synchronize()
+        got = dst.cpu().numpy().reshape(n, r.n_outs)
+        T = L.as_tuple()
+        for c in range(n):
+            x, shift = dict(fixed), 0
+            for name, b in zip(F.var_names, r.var_bits[:r.n_vars]):
+                x[name] = (c >> shift) & ((1 << b) - 1)
+                shift += b
+            assert tuple(int(v) for v in got[c]) == lo.apply(T, x), (fixed, x)
+    # a buffer one element short is refused before any launch
+    F = folded_cases(tg)[3][0].fold({"register": 3})
+    short = torch.zeros(((1 << F.raw.n_bits) * F.raw.n_outs - 1,), dtype=torch.int32, device="cuda")
+    assert tg._lib.tg_probe_folded_layout(ctypes.byref(F.raw), short.data_ptr(), short.numel() * 4,
+                                          None) == tg.TG_ERR_BUFFER

@@ -111,6 +111,20 @@ _sig("tg_layout_blocked", _int, _I2, _I2, _I2, _I2, _I2, _PP)
 _IP = ctypes.POINTER(_int)
 _sig("tg_layout_blocked_nd", _int, _int, _IP, _IP, _IP, _IP, _IP, _PP)
 _sig("tg_layout_cooperative", _int, _I2, _int, _I2, _PP)
+
+
+class tg_folded_layout(ctypes.Structure):
+    """include/tilegemm_layout_device.h: a layout folded for kernel evaluation."""
+    _fields_ = [("n_vars", _int), ("var_bits", _int * 8), ("n_bits", _int),
+                ("cols", ctypes.c_uint32 * 32), ("constant", ctypes.c_uint32), ("n_outs", _int),
+                ("out_shift", _int * 8), ("out_bits", _int * 8)]
+
+
+_sig("tg_layout_fold", _int, _vp, _int, ctypes.POINTER(_cp), ctypes.POINTER(ctypes.c_int32),
+     ctypes.POINTER(tg_folded_layout))
+_sig("tg_layout_folded_apply", _int, ctypes.POINTER(tg_folded_layout),
+     ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32))
+_sig("tg_probe_folded_layout", _int, ctypes.POINTER(tg_folded_layout), _vp, ctypes.c_size_t, _vp)
 _sig("tg_layout_register_tile", _int, _I2, _I2, _PP)
 _sig("tg_layout_swizzle128", _int, _int, _int, _PP)
 _sig("tg_layout_tmem_32x32b", _int, _int, _PP)
@@ -122,14 +136,15 @@ EXPORTED = [
     "tg_status_string", "tg_query_config",
     "tg_query_config_ws", "tg_query_config_for_sms",
     "tg_debug_status", "tg_debug_configure",
-    "tg_probe_swizzle128", "tg_probe_tmem_32x32b", "tg_layout_create", "tg_layout_destroy",
+    "tg_probe_swizzle128", "tg_probe_tmem_32x32b", "tg_probe_folded_layout",
+    "tg_layout_create", "tg_layout_destroy",
     "tg_layout_num_dims", "tg_layout_in_dim", "tg_layout_out_dim", "tg_layout_get_bases",
     "tg_layout_apply", "tg_layout_compose", "tg_layout_product", "tg_layout_sublayout",
     "tg_layout_transpose_outs", "tg_layout_transpose_ins", "tg_layout_reshape_ins",
     "tg_layout_reshape_outs", "tg_layout_divide_left", "tg_layout_divide_right",
     "tg_layout_rank", "tg_layout_is_injective",
     "tg_layout_is_surjective", "tg_layout_invert_and_compose", "tg_layout_blocked",
-    "tg_layout_blocked_nd",
+    "tg_layout_blocked_nd", "tg_layout_fold", "tg_layout_folded_apply",
     "tg_layout_cooperative", "tg_layout_register_tile", "tg_layout_swizzle128",
     "tg_layout_tmem_32x32b",
 ]
@@ -401,6 +416,17 @@ class LinearLayout:
         _check(_lib.tg_layout_apply(self._h, arr, out), "apply")
         return tuple(out[:nout])
 
+    def fold(self, fixed: dict) -> "FoldedLayout":
+        """Folds the inputs in ``fixed`` (name -> value) for kernel evaluation;
+        the other input dims stay variable, in the layout's order."""
+        names = list(fixed)
+        arr_n = (_cp * max(1, len(names)))(*[n.encode() for n in names])
+        arr_v = (ctypes.c_int32 * max(1, len(names)))(*[int(fixed[n]) for n in names])
+        f = tg_folded_layout()
+        _check(_lib.tg_layout_fold(self._h, len(names), arr_n, arr_v, ctypes.byref(f)), "fold")
+        var_names = [n for n, _ in self.in_dims if n not in fixed]
+        return FoldedLayout(f, var_names, [n for n, _ in self.out_dims])
+
     def compose(self, outer: "LinearLayout") -> "LinearLayout":
         return self._new(_lib.tg_layout_compose, self._h, outer._h, what="compose")
 
@@ -493,3 +519,19 @@ class LinearLayout:
     @classmethod
     def tmem_32x32b(cls, bn):
         return cls._new(_lib.tg_layout_tmem_32x32b, bn, what="tmem_32x32b")
+
+
+class FoldedLayout:
+    """A layout folded by tg_layout_fold: ``raw`` is the plain struct a kernel
+    takes; ``apply`` evaluates it on the host with the kernel's functions."""
+
+    def __init__(self, raw: tg_folded_layout, var_names: list, out_names: list):
+        self.raw = raw
+        self.var_names = var_names
+        self.out_names = out_names
+
+    def apply(self, vars: dict) -> tuple:
+        arr = (ctypes.c_int32 * max(1, len(self.var_names)))(*[vars[n] for n in self.var_names])
+        out = (ctypes.c_int32 * max(1, len(self.out_names)))()
+        _check(_lib.tg_layout_folded_apply(ctypes.byref(self.raw), arr, out), "folded_apply")
+        return tuple(out[:len(self.out_names)])

@@ -741,4 +741,71 @@ int tg_layout_tmem_32x32b(int bn, tg_layout** out) {
     });
 }
 
+int tg_layout_fold(const tg_layout* l, int n_fixed, const char* const* fixed_names,
+                   const int32_t* fixed_values, tg_folded_layout* out) {
+    if (!l || !out || n_fixed < 0 || (n_fixed > 0 && (!fixed_names || !fixed_values)))
+        return TG_ERR_INVALID_ARG;
+    return guarded([&] {
+        const size_t nin = l->in_names.size(), nout = l->out_names.size();
+        std::vector<int32_t> fixed(nin, 0);  // variable inputs stay 0: no part in the constant
+        std::vector<char> is_fixed(nin, 0);
+        for (int k = 0; k < n_fixed; ++k) {
+            if (!fixed_names[k]) throw LayoutError();
+            const int d = find(l->in_names, fixed_names[k]);
+            if (d < 0 || is_fixed[d]) throw LayoutError();
+            if (fixed_values[k] < 0 || fixed_values[k] >= (1 << l->in_bits[d])) throw LayoutError();
+            is_fixed[d] = 1;
+            fixed[d] = fixed_values[k];
+        }
+        if (nout > TG_FOLD_MAX_OUTS || total(l->out_bits) > 32) throw LayoutError();
+        tg_folded_layout f;
+        std::memset(&f, 0, sizeof(f));
+        f.n_outs = (int)nout;
+        int shift = 0;
+        for (size_t o = 0; o < nout; ++o) {
+            f.out_shift[o] = shift;
+            f.out_bits[o] = l->out_bits[o];
+            shift += l->out_bits[o];
+        }
+        // every output coordinate as a bit field of one word: XOR of words is
+        // XOR of every coordinate at once
+        auto pack = [&](const std::vector<int32_t>& c) {
+            uint32_t w = 0;
+            for (size_t o = 0; o < nout; ++o)
+                if (f.out_bits[o] > 0) w |= (uint32_t)c[o] << f.out_shift[o];
+            return w;
+        };
+        f.constant = pack(apply(*l, fixed.data()));
+        int row = 0;
+        for (size_t d = 0; d < nin; ++d) {
+            if (!is_fixed[d]) {
+                if (f.n_vars >= TG_FOLD_MAX_VARS || f.n_bits + l->in_bits[d] > TG_FOLD_MAX_BITS)
+                    throw LayoutError();
+                f.var_bits[f.n_vars++] = l->in_bits[d];
+                for (int i = 0; i < l->in_bits[d]; ++i) f.cols[f.n_bits++] = pack(l->bases[row + i]);
+            }
+            row += l->in_bits[d];
+        }
+        *out = f;
+        return TG_OK;
+    });
+}
+
+int tg_layout_folded_apply(const tg_folded_layout* f, const int32_t* vars, int32_t* outs) {
+    if (!f || (!vars && f->n_vars > 0) || (!outs && f->n_outs > 0)) return TG_ERR_INVALID_ARG;
+    if (f->n_vars < 0 || f->n_vars > TG_FOLD_MAX_VARS || f->n_outs < 0 ||
+        f->n_outs > TG_FOLD_MAX_OUTS || f->n_bits < 0 || f->n_bits > TG_FOLD_MAX_BITS)
+        return TG_ERR_LAYOUT;
+    uint32_t v[TG_FOLD_MAX_VARS] = {};
+    for (int k = 0; k < f->n_vars; ++k) {
+        if (f->var_bits[k] < 0 || f->var_bits[k] > 30 || vars[k] < 0 ||
+            vars[k] >= (1 << f->var_bits[k]))
+            return TG_ERR_INVALID_ARG;
+        v[k] = (uint32_t)vars[k];
+    }
+    const uint32_t packed = tg_folded_apply_packed(f, v);
+    for (int o = 0; o < f->n_outs; ++o) outs[o] = tg_folded_output(f, packed, o);
+    return TG_OK;
+}
+
 }  // extern "C"

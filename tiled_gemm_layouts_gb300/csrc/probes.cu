@@ -5,7 +5,10 @@
 //     offset can be compared with the (offset) -> (row, col) swizzle layout;
 //   * tg_probe_tmem_32x32b: one tcgen05.mma whose accumulator encodes its own
 //     coordinates (D[m][n] = 256 m + n), read back through tcgen05.ld 32x32b,
-//     so the (register, lane, warp) -> (m, n) readout layout can be checked.
+//     so the (register, lane, warp) -> (m, n) readout layout can be checked;
+//   * tg_probe_folded_layout: a folded layout (tilegemm_layout_device.h)
+//     evaluated by device code for every value of its variable inputs, so the
+//     kernel-side evaluation can be checked against the host module.
 // Every wait is bounded; a probe that gives up writes a status code.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -133,8 +136,28 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Thread c evaluates the folded layout at variable inputs split from c
+// (first variable dim in the lowest bits) and writes its n_outs outputs.
+__global__ void __launch_bounds__(256) folded_probe_kernel(const tg_folded_layout f, int32_t* dst) {
+    const uint32_t c = blockIdx.x * 256u + threadIdx.x;
+    if (c >= (1u << f.n_bits)) return;
+    uint32_t vars[TG_FOLD_MAX_VARS];
+    int shift = 0;
+#pragma unroll
+    for (int v = 0; v < TG_FOLD_MAX_VARS; ++v) {
+        const int b = v < f.n_vars ? f.var_bits[v] : 0;
+        vars[v] = b > 0 ? (c >> shift) & ((1u << b) - 1u) : 0u;
+        shift += b;
+    }
+    const uint32_t packed = tg_folded_apply_packed(&f, vars);
+    for (int o = 0; o < f.n_outs; ++o) dst[(size_t)c * f.n_outs + o] = tg_folded_output(&f, packed, o);
+}
+
 }  // namespace
 }  // namespace tg
+
+using namespace tg;
+
 
 using namespace tg;
 
@@ -192,4 +215,32 @@ extern "C" int tg_probe_tmem_32x32b(int bn, void* dst, int* status_dev, cudaStre
     }
     e = cudaGetLastError();
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+extern "C" int tg_probe_folded_layout(const tg_folded_layout* f, void* dst, size_t dst_bytes,
+                                      cudaStream_t stream) {
+    if (!f || !dst || f->n_vars < 0 || f->n_vars > TG_FOLD_MAX_VARS || f->n_bits < 0 ||
+        f->n_bits > 20 || f->n_outs < 1 || f->n_outs > TG_FOLD_MAX_OUTS)
+        return TG_ERR_INVALID_ARG;
+    int bits = 0;
+    for (int v = 0; v < f->n_vars; ++v) {
+        if (f->var_bits[v] < 0 || f->var_bits[v] > 20) return TG_ERR_INVALID_ARG;
+        bits += f->var_bits[v];
+    }
+    if (bits != f->n_bits) return TG_ERR_INVALID_ARG;
+    for (int o = 0; o < f->n_outs; ++o)
+        if (f->out_bits[o] < 0 || f->out_bits[o] > 30 || f->out_shift[o] < 0 ||
+            f->out_shift[o] + f->out_bits[o] > 32)
+            return TG_ERR_INVALID_ARG;
+    const size_t n = (size_t)1 << f->n_bits;
+    if (dst_bytes < n * f->n_outs * sizeof(int32_t)) return TG_ERR_BUFFER;
+    int dev = -1;
+    cudaPointerAttributes at;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaPointerGetAttributes(&at, dst) != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_POINTER;
+    }
+    if (at.type != cudaMemoryTypeDevice || at.device != dev) return TG_ERR_POINTER;
+    folded_probe_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(*f, static_cast<int32_t*>(dst));
+    return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
