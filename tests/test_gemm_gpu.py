@@ -114,6 +114,7 @@ def test_selector_reports_forced_configuration(tg):
 @pytest.mark.parametrize("M,N,K", [
     (184, 328, 264),  # ragged against every tile; dense strides stay 16-byte units
     (320, 448, 200),  # M, N whole 64-wide atoms (MN-major stages as one 3-D box), K ragged
+    (712, 696, 136),  # partial last atom in M and N: that CTA's stages use 2-D boxes, the rest 3-D
 ])
 def test_every_tile_configuration(tg, force, permA, permB, M, N, K):
     p = synthetic.gemm_problem(M, N, K, BF16, 31, permA=permA, permB=permB,
