@@ -57,6 +57,8 @@ CASES = [
      dict(bias=True, scale=True, relu=True, residual=True), 256),  # 8 blocks, every operand
     (777, 1001, 640, 1, 0, 5, 3, 1, dict(scale=True, residual=True), 512),
     (513, 300, 1000, 0, 0, 0, 0, 0, dict(bias=True), 4096),  # one block
+    (32, 2048, 512, 0, 0, 0, 0, 0, dict(scale=True), None),   # M <= 64: the swapped-operand path
+    (64, 1000, 3000, 1, 1, 0, 8, 2, dict(bias=True, residual=True, relu=True), None),
 ]
 
 
