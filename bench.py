@@ -298,6 +298,12 @@ class DevicePointwise:
         return n
 
 
+# the workloads reported beside the headline, in this order
+OTHER_WORKLOADS = ("bf16_4096", "fp16_8192x8192x4096_plain", "fp16_8192x8192x4096_fused",
+                   "fp16_4000x3000x1000_strided", "bf16_16384x1024x8192_scale",
+                   "bf16_32x16384x16384_scale")
+
+
 def time_kernel(fn, steps, warmup, flush_buf, stream):
     """Per-step kernel times (ms) by CUDA events on the launching stream, L2
     flushed before every step outside the event window."""
@@ -393,6 +399,9 @@ def main():
                     help="time only the two 8192 x 8192 pointwise programs (one JSON line)")
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the other workloads and the CPU baseline (for profiling)")
+    ap.add_argument("--profile-others", action="store_true",
+                    help="run each non-headline GEMM workload once after an L2 flush and exit "
+                         "(one launch per workload, for ncu captures; prints the launch order)")
     ap.add_argument("--workload", default="fp16_4096", help="headline workload key")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-stream-k", action="store_true",
@@ -430,6 +439,18 @@ def main():
                               "steps": args.steps, "warmup": args.warmup,
                               "peak_gbs": float(peaks.get("hbm_gbs", 6800.0)),
                               "workloads": lines}), flush=True)
+        return
+
+    if args.profile_others:
+        for key in OTHER_WORKLOADS:
+            dp = DeviceProblem(tg, make_problem(specs[key]), stream_k=not args.no_stream_k)
+            flush.fill_(1)
+            torch.cuda.synchronize()
+            dp.call(stream)
+            torch.cuda.synchronize()
+            if rank == 0:
+                print(json.dumps({"workload": key, "tile": dp.config}), flush=True)
+            del dp
         return
 
     # ---------------- headline: device-resident inputs
@@ -528,9 +549,7 @@ def main():
     # ---------------- other workloads (rank 0 reports; each replica runs them)
     if not args.headline_only:
         others = {}
-        for key in ("bf16_4096", "fp16_8192x8192x4096_plain", "fp16_8192x8192x4096_fused",
-                    "fp16_4000x3000x1000_strided", "bf16_16384x1024x8192_scale",
-                    "bf16_32x16384x16384_scale"):
+        for key in OTHER_WORKLOADS:
             p = make_problem(specs[key])
             dp = DeviceProblem(tg, p, stream_k=not args.no_stream_k)
             ts = time_kernel(dp.call, 10, 3, flush, stream)
