@@ -19,6 +19,10 @@ def test_benchmark_workload_choices(tg):
     assert (c["swap"], c["pair"], c["bm"], c["bn"], c["grid"]) == (0, 1, 256, 256, 152)
     c = cfg(tg, 8192, 8192, 4096, F16, 0, 0)
     assert (c["pair"], c["bn"], c["tiles"]) == (1, 256, 1024)
+    # 16384 x 1024 x 8192: 4 tile columns, so raster groups of 19 tile rows
+    # (76 tiles: one wave of CTA pairs)
+    c = cfg(tg, 16384, 1024, 8192, BF16, 0, 0)
+    assert (c["pair"], c["bn"], c["group_m"]) == (1, 256, 19)
     # K = 1000 (16 K-blocks) is too shallow for stream-K: both 256 x 256 (192
     # tiles) and 256 x 224 (224 tiles) take three whole waves and stage 256
     # B columns per tile; the narrower one computes fewer columns
@@ -51,7 +55,12 @@ def test_invariants(tg, seed):
         assert c["grid"] % 2 == 0 and c["grid"] // 2 <= c["tiles"]
     else:
         assert c["grid"] <= c["tiles"]
-    assert c["stages"] >= 4 and 1 <= c["group_m"] <= 16
+    # raster groups: 16 tile rows, widened to a whole wave when there are few
+    # tile columns, never more rows than the problem has
+    tiles_m, tiles_n = math.ceil(Mk / c["bm"]), math.ceil(Nk / c["bn"])
+    workers = c["grid"] // 2 if c["pair"] else c["grid"]
+    assert c["stages"] >= 4 and 1 <= c["group_m"] <= tiles_m
+    assert c["group_m"] == min(tiles_m, 16 if tiles_n * 16 >= workers else -(-workers // tiles_n))
     q_mn = (pa == 1) if c["swap"] else (pb == 0)
     assert not (c["bn"] == 32 and q_mn)
     assert c["swap"] == (1 if (M <= 64 and N > M) else 0)

@@ -54,7 +54,7 @@ struct Choice {
 };
 
 void apply_override(KernelConfig& c, bool& forced_bn, bool& forced_pair, bool& forced_swap,
-                    bool& forced_no_sk, bool& forced_sk) {
+                    bool& forced_no_sk, bool& forced_sk, bool& forced_group) {
     const char* env = std::getenv("TG_FORCE_CONFIG");
     if (!env || !*env) return;
     char buf[256];
@@ -72,6 +72,7 @@ void apply_override(KernelConfig& c, bool& forced_bn, bool& forced_pair, bool& f
             forced_pair = true;
         } else if (std::sscanf(tok, "group_m=%d", &v) == 1 && v >= 1 && v <= 64) {
             c.group_m = v;
+            forced_group = true;
         } else if (std::sscanf(tok, "grid=%d", &v) == 1 && v >= 1) {
             c.grid = v;
         } else if (std::sscanf(tok, "sk=%d", &v) == 1 && (v == 0 || v == 1)) {
@@ -102,8 +103,8 @@ KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int p
     // 8 at 8192 x 8192 x 4096 (less B re-read from DRAM) and 0.6 % at 4096^3.
     c.group_m = 16;
     bool forced_bn = false, forced_pair = false, forced_swap = false, forced_no_sk = false,
-         forced_sk = false;
-    apply_override(c, forced_bn, forced_pair, forced_swap, forced_no_sk, forced_sk);
+         forced_sk = false, forced_group = false;
+    apply_override(c, forced_bn, forced_pair, forced_swap, forced_no_sk, forced_sk, forced_group);
 
     // Stream-K only deals out tails of tiles at least 32 K-blocks deep (see
     // below), so only then may the wave estimate count on it.
@@ -164,6 +165,14 @@ KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int p
     const int slots = c.pair ? sms / 2 : sms;
     int clusters = c.grid > 0 ? (c.pair ? c.grid / 2 : c.grid) : slots;
     if (clusters > slots) clusters = slots;
+    // With few tile columns a group of 16 tile rows holds less than one wave:
+    // each wave then spans two groups and its A panels outgrow L2 before the
+    // next wave reuses them.  Widen the group to a whole wave of tiles
+    // (16384 x 1024 x 8192: 4 columns, groups of 19 rows, measured 4.5 %
+    // faster than 16, with 2.4x less A re-read from DRAM).
+    const int64_t tiles_n = cdiv(Nk, c.bn);
+    if (!forced_group && tiles_n * c.group_m < clusters) c.group_m = (int)cdiv(clusters, tiles_n);
+    if (c.group_m > tiles_m) c.group_m = (int)tiles_m;
     c.stages = gemm_stages(c.bn, c.pair);
 
     // Stream-K for the tail: the last partial wave plus one whole wave are
