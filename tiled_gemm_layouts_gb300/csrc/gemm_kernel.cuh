@@ -637,6 +637,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             // operands of the first run do not depend on the accumulator:
             // fetch them while the main loop still runs
             Aux cur, nxt;
+            if constexpr (AUX) {
+                // The residual rows of this warp's chunks are read only after
+                // the accumulator is ready: start moving them into L2 now,
+                // while the main loop still runs (one 64-byte run per lane and chunk).
+                if (whole && p.resid && !p.swap && rk < p.M) {
+                    const uint16_t* rrow = static_cast<const uint16_t*>(p.resid) + (long long)rk * p.ldr;
+                    for (int c = c_begin + 1; c < c_end; ++c) {
+                        const int c0 = tn * BN + c * 32;
+                        if (c0 < p.N) prefetch_global_l2(rrow + c0);
+                    }
+                }
+            }
             bool cur_full = (AUX && whole) ? prefetch_aux(p, rk, tn * BN + c_begin * 32, cur) : false;
             int ok = 1;
             if (lane == 0) ok = wait_bar(smem_addr(&tfull[buf]), aph, w, DEV_TIMEOUT_EPILOGUE);
