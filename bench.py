@@ -187,6 +187,8 @@ def workload_specs():
     """Synthetic workloads (seed = 1000 + index, draws in the order A, B, bias, scale, R)."""
     import synthetic as S
     return {
+        # the small case (launch latency: reported in microseconds, no roofline claim)
+        "fp16_128": dict(M=128, N=128, K=128, dtype=S.F16, seed=1001),
         "fp16_4096": dict(M=4096, N=4096, K=4096, dtype=S.F16, seed=1002),
         "bf16_4096": dict(M=4096, N=4096, K=4096, dtype=S.BF16, seed=1002),
         "fp16_4096x4096x8192": dict(M=4096, N=4096, K=8192, dtype=S.F16, seed=1002),
@@ -299,9 +301,57 @@ class DevicePointwise:
 
 
 # the workloads reported beside the headline, in this order
-OTHER_WORKLOADS = ("bf16_4096", "fp16_8192x8192x4096_plain", "fp16_8192x8192x4096_fused",
-                   "fp16_4000x3000x1000_strided", "bf16_16384x1024x8192_scale",
-                   "bf16_32x16384x16384_scale")
+OTHER_WORKLOADS = ("fp16_128", "bf16_4096", "fp16_8192x8192x4096_plain",
+                   "fp16_8192x8192x4096_fused", "fp16_4000x3000x1000_strided",
+                   "bf16_16384x1024x8192_scale", "bf16_32x16384x16384_scale")
+
+# the two 8192 x 8192 fp16 pointwise programs: row-major X with
+# relu(scale_m*X + bias_n) + R, and X given permuted with relu(scale_m*X + bias_n)
+POINTWISE_WORKLOADS = (("pointwise_fp16_8192x8192_scale_bias_relu_residual", 0),
+                       ("pointwise_fp16_8192x8192_permuted_input", 1))
+
+
+def make_pointwise(key):
+    import synthetic as S
+    permX = dict(POINTWISE_WORKLOADS)[key]
+    pp = S.pointwise_problem(8192, 8192, S.F16, 1020 + permX, permX=permX,
+                             bias=True, scale=True, residual=permX == 0)
+    pp["relu"] = True
+    return pp
+
+
+def decode_bits(bits, dtype):
+    """fp64 values of fp16 (numpy's half) or bf16 (widened to fp32) patterns."""
+    import numpy as np
+    bits = np.asarray(bits, dtype=np.uint16)
+    if dtype == 0:
+        return bits.view(np.float16).astype(np.float64)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def host_info() -> dict:
+    """The host the CPU oracle runs on: CPU model, machine, online cores."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu model")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return {"cpu_model": model or "unknown", "machine": platform.machine(),
+            "nproc": os.cpu_count()}
 
 
 def time_kernel(fn, steps, warmup, flush_buf, stream):
@@ -324,18 +374,62 @@ def time_kernel(fn, steps, warmup, flush_buf, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def oracle_sample_tflops(p, seconds: float, max_rows: int | None = None):
+def oracle_sample_tflops(p, seconds: float, max_rows: int | None = None, C=None):
     """The oracle as it stands on the first rows of the workload, in chunks of
-    16 rows until `seconds` have passed.  Returns (TFLOP/s, rows, seconds, threads)."""
+    16 rows until `seconds` have passed.  With C (the GPU's M x N result) every
+    element of those rows is also compared with the oracle (timed apart from
+    the oracle).  Returns (TFLOP/s, rows, seconds, threads, max normalised
+    error or None); raises on an element outside the parity tolerance."""
+    import numpy as np
     import oracle
-    rows, t0 = 0, time.perf_counter()
+    rows, spent, worst = 0, 0.0, None
+    got_all = None if C is None else C.cpu().numpy().view(np.uint16)
     limit = p["M"] if max_rows is None else min(p["M"], max_rows)
-    while rows < limit and time.perf_counter() - t0 < seconds:
+    while rows < limit and spent < seconds:
         r1 = min(limit, rows + 16)
-        oracle.gemm(p, rows=(rows, r1))
+        t0 = time.perf_counter()
+        ref = oracle.gemm(p, rows=(rows, r1))
+        spent += time.perf_counter() - t0
+        if got_all is not None:
+            got = decode_bits(got_all[rows:r1, :p["N"]], p["dtype"])
+            err = np.abs(got - ref) / np.maximum(1.0, np.abs(ref))
+            e = float(np.nanmax(err)) if np.all(np.isfinite(err)) else float("inf")
+            if not e <= 1e-2:
+                raise RuntimeError(f"GPU result differs from the oracle on rows {rows}..{r1}: "
+                                   f"max normalised error {e}")
+            worst = e if worst is None else max(worst, e)
         rows = r1
+    return 2.0 * rows * p["N"] * p["K"] / spent / 1e12, rows, spent, oracle.max_threads(), worst
+
+
+def oracle_rows_check(p, C, seed: int, block: int = 16) -> dict:
+    """CPU-baseline leg beside one GPU workload: the oracle as it stands on a
+    bounded sample of output rows -- all rows when M <= 64, else a block of
+    `block` rows at a seeded offset and the last `block` rows (the ragged edge)
+    -- timed on the host cores, and the GPU result C (the last timed call's
+    output, M x N) compared with it element by element on those rows.
+    Raises on any element outside |gpu - oracle| <= 1e-2 * max(1, |oracle|)."""
+    import numpy as np
+    import oracle
+    M, N, K = p["M"], p["N"], p["K"]
+    if M <= 2 * block:
+        spans = [(0, M)]
+    else:
+        r0 = int(np.random.default_rng(seed).integers(0, M - 2 * block))
+        spans = [(r0, r0 + block), (M - block, M)]
+    t0 = time.perf_counter()
+    ref = np.concatenate([oracle.gemm(p, rows=sp) for sp in spans])
     dt = time.perf_counter() - t0
-    return 2.0 * rows * p["N"] * p["K"] / dt / 1e12, rows, dt, oracle.max_threads()
+    rows = np.concatenate([np.arange(a, b) for a, b in spans])
+    got = decode_bits(C.cpu().numpy().view(np.uint16)[rows, :N], p["dtype"])
+    err = np.abs(got - ref) / np.maximum(1.0, np.abs(ref))
+    worst = float(np.nanmax(err)) if np.all(np.isfinite(err)) else float("inf")
+    if not worst <= 1e-2:
+        raise RuntimeError(f"GPU result differs from the oracle: max normalised error {worst} "
+                           f"on rows {spans}")
+    return {"rows": int(rows.size), "row_spans": spans, "seconds": dt,
+            "tflops": 2.0 * rows.size * N * K / dt / 1e12, "cores": oracle.max_threads(),
+            "max_norm_err": worst}
 
 
 def run_reference(args, world, rank):
@@ -362,24 +456,19 @@ def run_reference(args, world, rank):
         "data": "synthetic (SplitMix64 seed 1002, uniform[-1,1] rounded to fp16)",
         "config": {"workload": HEADLINE, "sample": f"{rows_per_step} rows of C per step"},
         "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{rows_per_step} of 4096 output rows per step, all K"},
+                         "sample": f"{rows_per_step} of 4096 output rows per step, all K",
+                         **host_info()},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
 def pointwise_lines(tg, flush, stream, peaks, steps, warmup) -> dict:
-    """The two 8192 x 8192 fp16 pointwise programs: row-major X with
-    relu(scale_m*X + bias_n) + R, and X given permuted with relu(scale_m*X +
-    bias_n).  GB/s of algorithmic bytes against the measured copy bandwidth."""
-    import synthetic as S
+    """The two 8192 x 8192 fp16 pointwise programs (POINTWISE_WORKLOADS).
+    GB/s of algorithmic bytes against the measured copy bandwidth."""
     out = {}
-    for key, permX in (("pointwise_fp16_8192x8192_scale_bias_relu_residual", 0),
-                       ("pointwise_fp16_8192x8192_permuted_input", 1)):
-        pp = S.pointwise_problem(8192, 8192, S.F16, 1020 + permX, permX=permX,
-                                 bias=True, scale=True, residual=permX == 0)
-        pp["relu"] = True
-        dpw = DevicePointwise(tg, pp)
+    for key, _ in POINTWISE_WORKLOADS:
+        dpw = DevicePointwise(tg, make_pointwise(key))
         ts = time_kernel(dpw.call, steps, warmup, flush, stream)
         t = statistics.median(ts) * 1e-3
         gbs = dpw.bytes() / t / 1e9
@@ -558,6 +647,12 @@ def main():
             entry = {"tflops": f / t / 1e12, "pct_dense_peak": 100 * f / t / 1e12 / peak,
                      "ms_median": t * 1e3,
                      "tile": dp.config}
+            if key == "fp16_128":
+                # launch latency bound: microseconds, no roofline claim
+                entry = {"us_median": t * 1e6, "us_min": min(ts) * 1e3, "tflops": f / t / 1e12,
+                         "tile": dp.config}
+            if rank == 0:
+                entry["oracle"] = oracle_rows_check(p, dp.C, specs[key]["seed"])
             if key.startswith("bf16_32x"):
                 gbs = algorithmic_bytes(p) / t / 1e9
                 entry.update({"gbs": gbs, "hbm_frac": gbs / float(peaks.get("hbm_gbs", 6800.0))})
@@ -568,11 +663,15 @@ def main():
         others.update(pointwise_lines(tg, flush, stream, peaks, 10, 3))
         line["workloads"] = others
         if rank == 0:
-            tfl, rows, secs, cores = oracle_sample_tflops(hp, args.cpu_seconds)
+            tfl, rows, secs, cores, worst = oracle_sample_tflops(hp, args.cpu_seconds, C=prob.C)
             line["cpu_baseline"] = {"value": tfl, "unit": "TFLOP/s", "cores": cores,
                                     "kind": "oracle",
                                     "sample": f"first {rows} of {M} output rows of the headline "
-                                              f"workload, all K ({secs:.1f} s)"}
+                                              f"workload, all K ({secs:.1f} s)",
+                                    **host_info()}
+            line["parity"] = {"oracle_rows": rows, "max_norm_err": worst, "tolerance": 1e-2,
+                              "checked": "last timed C of the headline against the oracle, "
+                                         "every element of those rows"}
     st, code = tg.tg_debug_status()
     if st != tg.TG_OK:
         raise RuntimeError(f"device watchdog fired during the bench: {code:#x}")

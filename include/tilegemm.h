@@ -11,6 +11,11 @@
  * error (ninetoothed.org "Named layouts", section "Runtime and compilation":
  * positive sizes and strides, non-contiguous inputs allowed, output storage
  * disjoint from every input, checks before kernel work).
+ *
+ * Per-device state (device attributes, the device address of the watchdog
+ * word and of the static scratch array, copy streams) is looked up once per
+ * device and cached for the life of the process; the library does not
+ * support cudaDeviceReset.
  */
 #ifndef TILEGEMM_H
 #define TILEGEMM_H
@@ -136,25 +141,32 @@ int tg_gemm_ws(int64_t M, int64_t N, int64_t K,
 
 /*
  * tg_gemm_ws without a caller workspace, for callers that cannot allocate
- * device memory: code running inside a CUDA stream capture (a cudaMalloc
- * there breaks the capture), code whose device memory is owned by an outside
- * allocator, or plugins whose host framework forbids allocations.  The pages
- * this library follows have no counterpart of this call; it exists for these
- * callers only.
+ * device memory: code under an outside allocator that owns all of the
+ * device's memory, plugins whose host framework forbids device allocations,
+ * and latency-bound host paths that cannot afford the implicit device
+ * synchronisation of cudaMalloc / cudaFree.  The pages this library follows
+ * have no counterpart of this call; it exists for these callers only.
  *
- * The stream-K scratch is one statically allocated device array of 40 MiB
- * (41943040 bytes) that every GPU loading this library keeps until the
- * process exits; nothing is allocated per call (no cudaMalloc, no cudaFree,
- * no allocating library routine).  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress): make that first call before
- * any stream capture on that device.  Each call zeroes the array's counters
- * on `stream` (cudaMemsetAsync) before its kernel.  Every call shares the
- * one array: calls whose kernels overlap on the GPU (other streams, other
- * host threads) race and corrupt each other's results -- serialise them.
+ * The scratch is one statically allocated device array of 64 MiB (67108864
+ * bytes) that every GPU loading this library keeps until the process exits;
+ * nothing is allocated per call (no cudaMalloc, no cudaFree, no allocating
+ * library routine).  It holds what tg_gemm_workspace_size_ex() reports for
+ * these arguments: the stream-K split's counters and partial sums, then the
+ * staging copies of operands a tensor map cannot describe (unaligned base or
+ * stride).  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it: make that first call before any
+ * stream capture on that device.  The library does not support
+ * cudaDeviceReset (the cached address may go stale).  When the call splits
+ * tiles, it zeroes the split's arrival counters on `stream`
+ * (cudaMemsetAsync) before its kernel.  Every call shares the one array:
+ * calls whose kernels overlap on the GPU (other streams, other host threads)
+ * race and corrupt each other's results -- serialise them.
  *
- * Arguments, checks and errors as tg_gemm_ws; TG_ERR_BUFFER when the split
- * would need more scratch than the array holds (tg_gemm_workspace_size()
- * above 41943040).  Shapes that need no split run whole tiles.
+ * Arguments, checks and errors as tg_gemm_ws; TG_ERR_BUFFER when the call
+ * needs more scratch than the array holds (tg_gemm_workspace_size_ex()
+ * above 67108864; every split the default selection makes on a 152-SM GPU
+ * fits, staging copies come on top).  Shapes that need neither a split nor staging run whole
+ * tiles and touch no scratch.
  */
 int tg_gemm_static_ws(int64_t M, int64_t N, int64_t K,
                       const void* A, int64_t lda, tg_perm permA,
@@ -222,9 +234,10 @@ int tg_gemm_host(int64_t M, int64_t N, int64_t K,
 
 /* Workspace bytes tg_gemm_host needs for this shape on the current device
  * (independent of the host strides; `epi` only says which epilogue operands
- * are present).  Errors as tg_gemm's shape and enum checks. */
-int tg_gemm_host_workspace_size(int64_t M, int64_t N, int64_t K, tg_perm permA, tg_perm permB,
-                                tg_dtype dtype, const tg_epilogue* epi, size_t* bytes);
+ * are present).  Arguments in tg_gemm_workspace_size's order.  Errors as
+ * tg_gemm's shape and enum checks. */
+int tg_gemm_host_workspace_size(int64_t M, int64_t N, int64_t K, tg_dtype dtype, tg_perm permA,
+                                tg_perm permB, const tg_epilogue* epi, size_t* bytes);
 
 /*
  * Pointwise program of the named-layout pages (ninetoothed.org "Named

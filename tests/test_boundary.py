@@ -161,9 +161,9 @@ def test_host_pipeline_checks_shape_before_the_device(tg):
     assert host(epi=tg.make_epilogue(relu=3)) == tg.TG_ERR_INVALID_ARG
     assert host() == tg.TG_ERR_UNSUPPORTED_DEVICE
     n = ctypes.c_size_t(0)
-    assert tg._lib.tg_gemm_host_workspace_size(256, 256, 256, 0, 0, F16, None, None) == \
+    assert tg._lib.tg_gemm_host_workspace_size(256, 256, 256, F16, 0, 0, None, None) == \
         tg.TG_ERR_INVALID_ARG
-    assert tg._lib.tg_gemm_host_workspace_size(0, 256, 256, 0, 0, F16, None, ctypes.byref(n)) == \
+    assert tg._lib.tg_gemm_host_workspace_size(0, 256, 256, F16, 0, 0, None, ctypes.byref(n)) == \
         tg.TG_ERR_INVALID_ARG
-    assert tg._lib.tg_gemm_host_workspace_size(256, 256, 256, 0, 0, F16, None, ctypes.byref(n)) == \
+    assert tg._lib.tg_gemm_host_workspace_size(256, 256, 256, F16, 0, 0, None, ctypes.byref(n)) == \
         tg.TG_ERR_UNSUPPORTED_DEVICE

@@ -1,7 +1,10 @@
 """tg_gemm_static_ws: the stream-K GEMM with library-owned static scratch, for
-callers that cannot allocate device memory (inside a stream capture, under an
-outside allocator).  Its results must match tg_gemm_ws with a caller
-workspace, call after call, although every call reuses the same array.
+callers that cannot allocate device memory (code under an outside allocator
+that owns the device's memory, plugins whose host framework forbids device
+allocations, host paths that cannot take cudaMalloc's implicit
+synchronisation).  Its results must match tg_gemm_ws with a caller workspace
+and the fp64 oracle, call after call, although every call reuses the same
+array.
 
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test."""
@@ -10,13 +13,14 @@ import os
 import numpy as np
 import pytest
 
+import oracle
 import synthetic
 from synthetic import F16, BF16
 from helpers import SENTINEL, check_close, decode, dev, host_bits
 
 pytestmark = pytest.mark.gpu
 
-CAPACITY = 40 << 20
+CAPACITY = 64 << 20
 
 
 class forced:
@@ -45,16 +49,20 @@ def operands(tg, p):
     return dev(p["A"]), dev(p["B"]), epi, (bias, scale, R)
 
 
+def args_of(p, A, B, C, epi):
+    return (p["M"], p["N"], p["K"], A, p["lda"], p["permA"], B, p["ldb"], p["permB"], C,
+            p["N"], p["dtype"], epi)
+
+
 def with_workspace(tg, p):
-    """Reference: the existing entry point with a caller-allocated workspace."""
+    """The existing entry point, with a workspace the caller allocates."""
     import torch
     A, B, epi, keep = operands(tg, p)
-    M, N, K = p["M"], p["N"], p["K"]
-    need = tg.tg_gemm_workspace_size(M, N, K, p["dtype"], p["permA"], p["permB"], epi)
+    C = torch.full((p["M"], p["N"]), SENTINEL, dtype=torch.int16, device="cuda")
+    args = args_of(p, A, B, C, epi)
+    need = tg.tg_gemm_workspace_size_ex(*args)
     ws = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
-    C = torch.full((M, N), SENTINEL, dtype=torch.int16, device="cuda")
-    rc = tg.tg_gemm_ws(M, N, K, A, p["lda"], p["permA"], B, p["ldb"], p["permB"], C, N,
-                       p["dtype"], epi, ws if need else None, need)
+    rc = tg.tg_gemm_ws(*args, ws if need else None, need)
     torch.cuda.synchronize()
     assert rc == tg.TG_OK, tg.tg_status_string(rc)
     return host_bits(C), need
@@ -63,10 +71,8 @@ def with_workspace(tg, p):
 def static_scratch(tg, p):
     import torch
     A, B, epi, keep = operands(tg, p)
-    M, N, K = p["M"], p["N"], p["K"]
-    C = torch.full((M, N), SENTINEL, dtype=torch.int16, device="cuda")
-    rc = tg.tg_gemm_static_ws(M, N, K, A, p["lda"], p["permA"], B, p["ldb"], p["permB"], C, N,
-                              p["dtype"], epi)
+    C = torch.full((p["M"], p["N"]), SENTINEL, dtype=torch.int16, device="cuda")
+    rc = tg.tg_gemm_static_ws(*args_of(p, A, B, C, epi))
     torch.cuda.synchronize()
     assert rc == tg.TG_OK, tg.tg_status_string(rc)
     st, code = tg.tg_debug_status()
@@ -74,8 +80,10 @@ def static_scratch(tg, p):
     return host_bits(C)
 
 
-def same_within_tolerance(got, ref, dtype, what):
-    check_close(got, decode(ref, dtype), dtype, what=what)
+def agree(got, ref_bits, want, dtype, what):
+    """Within the parity tolerance of the caller-workspace call and of the oracle."""
+    check_close(got, decode(ref_bits, dtype), dtype, what=f"{what} vs tg_gemm_ws")
+    check_close(got, want, dtype, what=f"{what} vs oracle")
 
 
 def test_static_scratch_matches_caller_workspace_two_calls_in_a_row(tg):
@@ -88,30 +96,46 @@ def test_static_scratch_matches_caller_workspace_two_calls_in_a_row(tg):
     ]
     cases[1][0]["relu"] = True
     for p, cfg in cases:
+        want = oracle.gemm(p)
         with forced(cfg):
             ref, need = with_workspace(tg, p)
             assert 0 < need <= CAPACITY  # the case really uses scratch
             first = static_scratch(tg, p)
             second = static_scratch(tg, p)
-        same_within_tolerance(first, ref, p["dtype"], f"{cfg}, first call")
-        same_within_tolerance(second, ref, p["dtype"], f"{cfg}, second call")
+        agree(first, ref, want, p["dtype"], f"{cfg}, first call")
+        agree(second, ref, want, p["dtype"], f"{cfg}, second call")
+
+
+def test_static_scratch_stages_unaligned_operands(tg):
+    # a row stride that is not a whole number of 16-byte units: B is copied
+    # into an aligned image inside the static array, after the split's region
+    p = synthetic.gemm_problem(640, 264, 960, F16, 304, ldb=264 + 3, bias=True)
+    want = oracle.gemm(p)
+    with forced("pair=0,bn=128,grid=6,sk=1"):
+        ref, need = with_workspace(tg, p)
+        assert need > tg.tg_gemm_workspace_size(640, 264, 960, F16)  # staging on top of the split
+        first = static_scratch(tg, p)
+        second = static_scratch(tg, p)
+    agree(first, ref, want, F16, "unaligned ldb, first call")
+    agree(second, ref, want, F16, "unaligned ldb, second call")
 
 
 def test_static_scratch_default_selection_headline_shape(tg):
     # the 4096^3 fp16 GEMM picks a stream-K split whose scratch fits the array
     p = synthetic.gemm_problem(4096, 4096, 4096, F16, 1002)
+    want = oracle.gemm(p)
     with forced(None):
         ref, need = with_workspace(tg, p)
         assert 0 < need <= CAPACITY
         for call in ("first", "second"):
             got = static_scratch(tg, p)
-            same_within_tolerance(got, ref, F16, f"4096^3, {call} call")
+            agree(got, ref, want, F16, f"4096^3, {call} call")
 
 
 def test_static_scratch_rejects_splits_beyond_capacity(tg):
     import torch
-    # 16 CTA-pair tiles dealt out over 76 clusters: six partial slots per
-    # split tile, about 114 MB of scratch, more than the static array holds
+    # 16 CTA-pair tiles forced to be dealt out over 76 clusters: six partial
+    # slots per split tile, about 120 MB of scratch, more than the array holds
     p = synthetic.gemm_problem(1024, 1024, 4096, F16, 303)
     A, B, epi, keep = operands(tg, p)
     C = torch.zeros((1024, 1024), dtype=torch.int16, device="cuda")

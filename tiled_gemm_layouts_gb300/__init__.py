@@ -250,7 +250,7 @@ def gemm_host(M, N, K, A, lda, permA, B, ldb, permB, C, ldc, dtype, epi, workspa
 
 def tg_gemm_host_workspace_size(M, N, K, dtype, permA=TG_OP_N, permB=TG_OP_N, epi=None) -> int:
     n = ctypes.c_size_t(0)
-    rc = _lib.tg_gemm_host_workspace_size(M, N, K, permA, permB, dtype,
+    rc = _lib.tg_gemm_host_workspace_size(M, N, K, dtype, permA, permB,
                                           ctypes.byref(epi) if epi is not None else None,
                                           ctypes.byref(n))
     if rc != TG_OK:

@@ -448,7 +448,7 @@ int gemm_impl(const Args& user, void* workspace, size_t ws_bytes, cudaStream_t s
     p.sk_cmax = cfg.sk_cmax;
     p.sk_iters = (long long)cfg.sk_tiles * p.num_kb;
     if (cfg.sk_tiles > 0) {
-        const long long counters = ((long long)p.workers * 2 * 4 + 255) / 256 * 256;
+        const long long counters = sk_counter_bytes(p.workers);
         p.ws_count = static_cast<int*>(workspace);
         p.ws_partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + counters);
     }
@@ -620,6 +620,20 @@ extern "C" int tg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, tg_dtype 
     *bytes = (size_t)c.ws_bytes;
     return TG_OK;
 }
+
+namespace tg {
+int split_counter_bytes(int64_t M, int64_t N, int64_t K, int dtype, int permA, int permB,
+                        bool has_epilogue, size_t* bytes) {
+    int rc = check_shape(M, N, K, dtype, permA, permB, nullptr);
+    if (rc) return rc;
+    int dev;
+    DeviceInfo* info;
+    if ((rc = current_device(&dev, &info))) return rc;
+    const KernelConfig c = select_config(M, N, K, dtype, permA, permB, has_epilogue, info->sms, true);
+    *bytes = c.sk_tiles > 0 ? (size_t)sk_counter_bytes(c.pair ? c.grid / 2 : c.grid) : 0;
+    return TG_OK;
+}
+}  // namespace tg
 
 extern "C" const char* tg_status_string(int status) {
     switch (status) {

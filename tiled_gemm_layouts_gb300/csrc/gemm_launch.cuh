@@ -1,6 +1,8 @@
 // gemm_launch.cuh -- the set of compiled tile configurations and their launch.
 #pragma once
 
+#include <atomic>
+
 #include "gemm_kernel.cuh"
 
 // Every (BN, PAIR) the library is compiled for: single-CTA 128 x BN tiles and
@@ -21,9 +23,17 @@ cudaError_t launch_config(const GemmParams& p, const KernelConfig& cfg, cudaStre
                                           cudaStream_t stream) {                          \
         using TS = TileShape<B, P>;                                                       \
         auto kern = gemm_kernel<B, P, X, S>;                                              \
-        cudaError_t e = cudaFuncSetAttribute(                                             \
-            kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TS::kSmemBytes);           \
+        static std::atomic<unsigned long long> attr_set{0}; /* one bit per device */     \
+        int dev = 0;                                                                      \
+        cudaError_t e = cudaGetDevice(&dev);                                              \
         if (e != cudaSuccess) return e;                                                   \
+        const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;                    \
+        if (!(attr_set.load(std::memory_order_acquire) & bit)) {                          \
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                                     TS::kSmemBytes);                                     \
+            if (e != cudaSuccess) return e;                                               \
+            attr_set.fetch_or(bit, std::memory_order_release);                            \
+        }                                                                                 \
         cudaLaunchConfig_t lc = {};                                                       \
         cudaLaunchAttribute attr[1];                                                      \
         lc.gridDim = dim3(cfg.grid, 1, 1);                                                \

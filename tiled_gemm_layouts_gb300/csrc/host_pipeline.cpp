@@ -214,8 +214,8 @@ T* at(void* base, size_t off) {
 
 }  // namespace
 
-extern "C" int tg_gemm_host_workspace_size(int64_t M, int64_t N, int64_t K, tg_perm permA,
-                                           tg_perm permB, tg_dtype dtype, const tg_epilogue* epi,
+extern "C" int tg_gemm_host_workspace_size(int64_t M, int64_t N, int64_t K, tg_dtype dtype,
+                                           tg_perm permA, tg_perm permB, const tg_epilogue* epi,
                                            size_t* bytes) {
     if (!bytes) return TG_ERR_INVALID_ARG;
     Plan p;

@@ -2,33 +2,34 @@
 // fixed, statically allocated device array, for callers that cannot allocate
 // device memory themselves.
 //
-// Who needs it: code that runs where cudaMalloc is not an option -- inside a
-// CUDA stream capture (a cudaMalloc there breaks the capture), under an
-// external allocator that owns all device memory, or in a plugin whose host
-// framework forbids device allocations.  Such callers can still pass their
-// inputs and outputs, but not the workspace tg_gemm_ws asks for.
+// Who needs it: code for which cudaMalloc is not an option -- code under an
+// outside allocator that owns all of the device's memory (a framework's
+// memory pool), plugins whose host framework forbids device allocations, and
+// latency-bound host paths that cannot afford the implicit device
+// synchronisation a cudaMalloc or cudaFree may cause.  Such callers can still
+// pass their inputs and outputs, but not the workspace tg_gemm_ws asks for.
 //
 // The scratch lives in one file-scope __device__ array of kScratchBytes that
 // every GPU loading this library keeps until the process exits.  In host code
 // the array's name is only a stand-in symbol, never a device address: the
 // address is looked up once per device with cudaGetSymbolAddress (with that
-// device current) and cached.
+// device current) and cached.  The library does not support cudaDeviceReset:
+// after one, the cached address may be stale.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <mutex>
 
 #include "../../include/tilegemm.h"
+#include "select.h"
 
 namespace {
 
-// 40 MiB: enough for the stream-K split of every 256 x 256 CTA-pair tiling on
-// a 152-SM GPU with two contributors per split tile (76 clusters x 2 slots x
-// 256 KB plus counters, 39.8 MB).
-constexpr size_t kScratchBytes = size_t(40) << 20;
-// The arrival counters sit at the start of the workspace; they must be zero
-// when a launch starts.  They occupy at most this many bytes for any split.
-constexpr size_t kCounterBytes = 4096;
+// 64 MiB: enough for every stream-K split the default selection makes on a
+// 152-SM GPU -- at most three partial slots per worker of at most 256 x 256
+// fp32 per cluster (76 x 3 x 256 KB plus counters, 59.8 MB) -- and for the
+// staging copies of unaligned operands of smaller problems.
+constexpr size_t kScratchBytes = size_t(64) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -65,18 +66,27 @@ extern "C" int tg_gemm_static_ws(int64_t M, int64_t N, int64_t K, const void* A,
                                  tg_perm permA, const void* B, int64_t ldb, tg_perm permB,
                                  void* C, int64_t ldc, tg_dtype dtype, const tg_epilogue* epi,
                                  cudaStream_t stream) {
+    // The whole scratch this call needs: the split's counters and partial
+    // sums, then staging copies of operands a tensor map cannot describe.
     size_t need = 0;
     int rc = tg_gemm_workspace_size_ex(M, N, K, A, lda, permA, B, ldb, permB, C, ldc, dtype, epi,
                                        &need);
     if (rc != TG_OK) return rc;
     if (need > kScratchBytes) return TG_ERR_BUFFER;  // more scratch than the static array holds
+    size_t counters = 0;
+    const bool has_epi = epi && (epi->bias_n || epi->scale_m || epi->residual || epi->relu);
+    if ((rc = tg::split_counter_bytes(M, N, K, (int)dtype, (int)permA, (int)permB, has_epi,
+                                      &counters)) != TG_OK)
+        return rc;
+    if (counters > need) return TG_ERR_CUDA;  // inconsistent sizes: never launch on them
     void* scratch = nullptr;
     if ((rc = scratch_address(&scratch)) != TG_OK) return rc;
-    if (need > 0) {
-        // The array keeps whatever the previous call left: zero the counters
-        // (in stream order, before this call's kernel reads them).
-        if (cudaMemsetAsync(scratch, 0, need < kCounterBytes ? need : kCounterBytes, stream) !=
-            cudaSuccess) {
+    if (counters > 0) {
+        // The array keeps whatever the previous call left: zero the split's
+        // arrival counters (in stream order, before this call's kernel reads
+        // them).  The partial-sum slots and staging copies are always written
+        // before they are read.
+        if (cudaMemsetAsync(scratch, 0, counters, stream) != cudaSuccess) {
             cudaGetLastError();
             return TG_ERR_CUDA;
         }

@@ -57,9 +57,15 @@ void apply_override(KernelConfig& c, bool& forced_bn, bool& forced_pair, bool& f
                     bool& forced_no_sk, bool& forced_sk, bool& forced_group) {
     const char* env = std::getenv("TG_FORCE_CONFIG");
     if (!env || !*env) return;
-    char buf[256];
-    std::snprintf(buf, sizeof(buf), "%s", env);
-    for (char* tok = std::strtok(buf, ", "); tok; tok = std::strtok(nullptr, ", ")) {
+    // Tokens are split by hand (no strtok: this runs on every call, possibly
+    // from several host threads at once).
+    std::string spec(env);
+    for (size_t i = 0; i < spec.size();) {
+        const size_t j = spec.find_first_of(", ", i);
+        const std::string word = spec.substr(i, j == std::string::npos ? std::string::npos : j - i);
+        i = j == std::string::npos ? spec.size() : j + 1;
+        if (word.empty()) continue;
+        const char* tok = word.c_str();
         int v = 0;
         if (std::sscanf(tok, "bn=%d", &v) == 1 && gemm_stages(v, 0) > 0) {
             c.bn = v;
@@ -184,9 +190,16 @@ KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int p
     // Measured on GB300: the split pays when whole waves leave at least 10 %
     // of the SM-time idle, every worker also has whole tiles, and tiles are
     // at least 32 K-blocks deep (the partial sums cost about half a tile).
+    // A problem with fewer tiles than workers (less than one wave) is split
+    // too when the tiles fill at least half the workers: every worker then
+    // takes an equal K-range and no tile has more than three contributors
+    // (32 x 16384 x 16384, 128 tiles of 128 x 32 on 152 SMs: every SM streams
+    // its share of B instead of 24 of them idling).
     const double wave_fill = (double)tiles / ((double)cdiv(tiles, clusters) * clusters);
-    const bool want_sk = forced_sk ? tiles % clusters != 0
-                                   : (tiles > clusters && wave_fill < 0.9 && num_kb >= 32);
+    const bool tail_split = tiles > clusters && wave_fill < 0.9 && num_kb >= 32;
+    const bool subwave_split = tiles < clusters && 2 * tiles >= clusters && wave_fill < 0.9 &&
+                               num_kb >= 32;
+    const bool want_sk = forced_sk ? tiles % clusters != 0 : (tail_split || subwave_split);
     if (allow_sk && !forced_no_sk && want_sk) {
         const int64_t sk_tiles = tiles > clusters ? clusters + tiles % clusters : tiles;
         const int64_t iters = sk_tiles * num_kb;
@@ -205,9 +218,10 @@ KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int p
     return c;
 }
 
+long long sk_counter_bytes(int workers) { return ((long long)workers * 2 * 4 + 255) / 256 * 256; }
+
 long long sk_workspace_bytes(int workers, int cmax, int bm, int bn) {
-    const long long counters = ((long long)workers * 2 * 4 + 255) / 256 * 256;
-    return counters + (long long)workers * cmax * bm * bn * 4;
+    return sk_counter_bytes(workers) + (long long)workers * cmax * bm * bn * 4;
 }
 
 std::string describe_config(const KernelConfig& c) {

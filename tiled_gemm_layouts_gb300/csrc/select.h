@@ -21,6 +21,16 @@ KernelConfig select_config(int64_t M, int64_t N, int64_t K, int dtype, int permA
 // accumulator slots.
 long long sk_workspace_bytes(int workers, int cmax, int bm, int bn);
 
+// Bytes of the arrival counters at the start of a split's workspace (two
+// ints per worker, rounded up to 256 bytes); they are zero between calls.
+long long sk_counter_bytes(int workers);
+
 std::string describe_config(const KernelConfig& c);
+
+// Bytes of stream-K arrival counters that tg_gemm_ws would use at the start
+// of its workspace for these arguments on the current device (0 when the
+// selector runs whole tiles only).  Status as tg_gemm_workspace_size.
+int split_counter_bytes(int64_t M, int64_t N, int64_t K, int dtype, int permA, int permB,
+                        bool has_epilogue, size_t* bytes);
 
 }  // namespace tg
