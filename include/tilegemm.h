@@ -147,7 +147,7 @@ int tg_gemm_ws(int64_t M, int64_t N, int64_t K,
  * synchronisation of cudaMalloc / cudaFree.  The pages this library follows
  * have no counterpart of this call; it exists for these callers only.
  *
- * The scratch is one statically allocated device array of 64 MiB (67108864
+ * The scratch is one statically allocated device array of 40 MiB (41943040
  * bytes) that every GPU loading this library keeps until the process exits;
  * nothing is allocated per call (no cudaMalloc, no cudaFree, no allocating
  * library routine).  It holds what tg_gemm_workspace_size_ex() reports for
@@ -164,7 +164,7 @@ int tg_gemm_ws(int64_t M, int64_t N, int64_t K,
  *
  * Arguments, checks and errors as tg_gemm_ws; TG_ERR_BUFFER when the call
  * needs more scratch than the array holds (tg_gemm_workspace_size_ex()
- * above 67108864; every split the default selection makes on a 152-SM GPU
+ * above 41943040; every split the default selection makes on a 152-SM GPU
  * fits, staging copies come on top).  Shapes that need neither a split nor staging run whole
  * tiles and touch no scratch.
  */

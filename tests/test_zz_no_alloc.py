@@ -20,7 +20,7 @@ from helpers import SENTINEL, check_close, decode, dev, host_bits
 
 pytestmark = pytest.mark.gpu
 
-CAPACITY = 64 << 20
+CAPACITY = 40 << 20
 
 
 class forced:
@@ -135,7 +135,7 @@ def test_static_scratch_default_selection_headline_shape(tg):
 def test_static_scratch_rejects_splits_beyond_capacity(tg):
     import torch
     # 16 CTA-pair tiles forced to be dealt out over 76 clusters: six partial
-    # slots per split tile, about 120 MB of scratch, more than the array holds
+    # slots per split tile, about 114 MB of scratch, more than the array holds
     p = synthetic.gemm_problem(1024, 1024, 4096, F16, 303)
     A, B, epi, keep = operands(tg, p)
     C = torch.zeros((1024, 1024), dtype=torch.int16, device="cuda")

@@ -25,11 +25,11 @@
 
 namespace {
 
-// 64 MiB: enough for every stream-K split the default selection makes on a
-// 152-SM GPU -- at most three partial slots per worker of at most 256 x 256
-// fp32 per cluster (76 x 3 x 256 KB plus counters, 59.8 MB) -- and for the
-// staging copies of unaligned operands of smaller problems.
-constexpr size_t kScratchBytes = size_t(64) << 20;
+// 40 MiB: enough for every stream-K split the default selection makes on a
+// 152-SM GPU -- the tail after whole waves, two partial slots per worker of at
+// most 256 x 256 fp32 per cluster (76 x 2 x 256 KB plus counters, 39.8 MB) --
+// and for the staging copies of unaligned operands of smaller problems.
+constexpr size_t kScratchBytes = size_t(40) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 

@@ -129,6 +129,33 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
         : "memory");
 }
 
+// An L2 cache policy that marks the lines it touches as the first to evict
+// (for data read or written once: the residual and the output tiles).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_store_2d with an L2 cache policy for the written lines.
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, uint32_t src, int32_t c0,
+                                                  int32_t c1, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+        " [%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "l"(pol)
+        : "memory");
+}
+
+// 16-byte read-only global load with an L2 cache policy.
+__device__ __forceinline__ uint4 ld_nc_hint(const void* ptr, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr), "l"(pol));
+    return v;
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -190,16 +190,14 @@ KernelConfig select_config(int64_t M, int64_t N, int64_t K, int /*dtype*/, int p
     // Measured on GB300: the split pays when whole waves leave at least 10 %
     // of the SM-time idle, every worker also has whole tiles, and tiles are
     // at least 32 K-blocks deep (the partial sums cost about half a tile).
-    // A problem with fewer tiles than workers (less than one wave) is split
-    // too when the tiles fill at least half the workers: every worker then
-    // takes an equal K-range and no tile has more than three contributors
-    // (32 x 16384 x 16384, 128 tiles of 128 x 32 on 152 SMs: every SM streams
-    // its share of B instead of 24 of them idling).
+    // A problem with fewer tiles than workers is not split: dealing every
+    // tile out over all workers measured slower on GB300 (32 x 16384 x 16384
+    // on 152 instead of 128 SMs: 5.05 against 5.31 TB/s; 2048 x 2048 x 4096:
+    // 729 against 1049 TFLOP/s) -- every tile then ends in a fix-up, all at
+    // the end of the launch.
     const double wave_fill = (double)tiles / ((double)cdiv(tiles, clusters) * clusters);
-    const bool tail_split = tiles > clusters && wave_fill < 0.9 && num_kb >= 32;
-    const bool subwave_split = tiles < clusters && 2 * tiles >= clusters && wave_fill < 0.9 &&
-                               num_kb >= 32;
-    const bool want_sk = forced_sk ? tiles % clusters != 0 : (tail_split || subwave_split);
+    const bool want_sk = forced_sk ? tiles % clusters != 0
+                                   : (tiles > clusters && wave_fill < 0.9 && num_kb >= 32);
     if (allow_sk && !forced_no_sk && want_sk) {
         const int64_t sk_tiles = tiles > clusters ? clusters + tiles % clusters : tiles;
         const int64_t iters = sk_tiles * num_kb;
