@@ -44,7 +44,18 @@
 
 namespace tg {
 
-constexpr int kBK = 64;        // K elements per stage: one 128-byte swizzle row of fp16/bf16
+constexpr int kBK = 64;        // K elements per ring slot: one 128-byte swizzle row of fp16/bf16
+// K-blocks per barrier transaction in whole-tile kernels: two consecutive
+// ring slots fill and drain together under one full/empty barrier pair.  Each
+// transaction has a fixed cost beside its bytes (a bare TMA stream of 64 KB
+// transactions measured 64.8 B/clk per SM where 32 KB ones reached 39.6), and
+// pairs measured +2.5 % at 8192 x 8192 x 4096.  Stream-K kernels keep one
+// K-block per transaction: their K-ranges start and end anywhere, and pairs
+// measured 1-2 % slower there.
+template <bool SK>
+struct KBlocksPerStage {
+    static constexpr int value = SK ? 1 : 2;
+};
 constexpr int kUmmaK = 16;     // K per tcgen05.mma of kind::f16
 constexpr int kEpiWarps = 4;   // one epilogue warp per TMEM lane quadrant (8 measured no faster overall)
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, epilogue warps
@@ -67,6 +78,7 @@ struct TileShape {
                                    : 2 * BN <= 256 ? 256 : 512;
     static constexpr int kSmemBytes = 1024 + kStages * kStage + kStaging + (2 * kStages + 5) * 8 + 16;
     static_assert(kStages >= 4, "too few pipeline stages");
+    static_assert(kStages % 2 == 0, "ring slots come in whole barrier groups");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN: multiple of 32 in 32..256");
     static_assert(!PAIR || BN % 32 == 0, "pair tiles split BN in halves of 16-multiples");
@@ -409,6 +421,7 @@ template <int BN, bool PAIR, bool AUX, bool SK>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
     using TS = TileShape<BN, PAIR>;
     constexpr int STAGES = TS::kStages;
+    constexpr int kKPerStage = KBlocksPerStage<SK>::value;
     constexpr int CG = PAIR ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128B-swizzle atoms (same offset in both CTAs of a pair)
@@ -467,12 +480,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            int stage = 0;
+            // Slots are filled kKPerStage at a time: group q holds slots
+            // q*kKPerStage.. and one full/empty barrier pair; a work item's
+            // last group may hold fewer K-blocks.
+            constexpr int GROUPS = STAGES / kKPerStage;
+            int grp = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
             long long g = 0;
             bool ok = true;
-            // bytes this CTA lands per stage (A half + its B columns)
+            // bytes this CTA lands per K-block (A half + its B columns)
             const uint32_t a_bytes = TS::kAStage;
             const uint32_t b_bytes = p.q_mn_major ? (uint32_t)TS::kBStage : (uint32_t)TS::kBNC * 128u;
             const uint32_t stage_tx = (a_bytes + b_bytes) * (PAIR ? 2u : 1u);
@@ -483,79 +500,87 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 tile_coords(p, t, tm, tn);
                 const int m0 = tm * TS::kBM + (int)rank * 128;
                 const int n0 = tn * BN + (int)rank * TS::kBNC;
-                for (int kb = kb0; kb < kb1; ++kb, ++g) {
-                    if (!wait_bar(smem_addr(&empty[stage]), phase ^ 1, w, DEV_TIMEOUT_PRODUCER)) {
+                for (int kb = kb0; kb < kb1; kb += kKPerStage) {
+                    const int n = kb1 - kb < kKPerStage ? kb1 - kb : kKPerStage;
+                    if (!wait_bar(smem_addr(&empty[grp]), phase ^ 1, w, DEV_TIMEOUT_PRODUCER)) {
                         ok = false;
                         break;
                     }
-                    if (g != p.inject_skip_load) {
-                        const uint32_t fb_local = smem_addr(&full[stage]);
+                    if (p.inject_skip_load < g || p.inject_skip_load >= g + n) {
+                        const uint32_t fb_local = smem_addr(&full[grp]);
                         if (leader) {
-                            mbar_arrive_expect_tx(fb_local, stage_tx);
-                            armed |= 1u << stage;
-                            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                            mbar_arrive_expect_tx(fb_local, stage_tx * (uint32_t)n);
+                            armed |= 1u << grp;
+                            armed_parity = (armed_parity & ~(1u << grp)) | (phase << grp);
                         }
                         const uint32_t fb = PAIR ? mapa_shared(fb_local, 0) : fb_local;
-                        const uint32_t a_dst = smem_addr(sA + stage * TS::kAStage);
-                        const uint32_t b_dst = smem_addr(sB + stage * TS::kBStage);
-                        const int k0 = kb * kBK;
-                        if (p.p_3d) {
-                            if constexpr (PAIR)
-                                tma_load_3d_pair(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
-                            else
-                                tma_load_3d(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
-                        } else if (p.p_mn_major) {
 #pragma unroll
-                            for (int j = 0; j < 2; ++j) {
+                        for (int j = 0; j < kKPerStage; ++j) {
+                            if (j >= n) break;
+                            const int slot = grp * kKPerStage + j;
+                            const uint32_t a_dst = smem_addr(sA + slot * TS::kAStage);
+                            const uint32_t b_dst = smem_addr(sB + slot * TS::kBStage);
+                            const int k0 = (kb + j) * kBK;
+                            if (p.p_3d) {
                                 if constexpr (PAIR)
-                                    tma_load_2d_pair(a_dst + j * 8192, &p.map_p, fb, m0 + 64 * j, k0);
+                                    tma_load_3d_pair(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
                                 else
-                                    tma_load_2d(a_dst + j * 8192, &p.map_p, fb, m0 + 64 * j, k0);
-                            }
-                        } else {
-                            if constexpr (PAIR)
-                                tma_load_2d_pair(a_dst, &p.map_p, fb, k0, m0);
-                            else
-                                tma_load_2d(a_dst, &p.map_p, fb, k0, m0);
-                        }
-                        if (p.q_3d) {
-                            if constexpr (PAIR)
-                                tma_load_3d_pair(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
-                            else
-                                tma_load_3d(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
-                        } else if (p.q_mn_major) {
+                                    tma_load_3d(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
+                            } else if (p.p_mn_major) {
 #pragma unroll
-                            for (int j = 0; j < TS::kBBoxes; ++j) {
+                                for (int h = 0; h < 2; ++h) {
+                                    if constexpr (PAIR)
+                                        tma_load_2d_pair(a_dst + h * 8192, &p.map_p, fb, m0 + 64 * h, k0);
+                                    else
+                                        tma_load_2d(a_dst + h * 8192, &p.map_p, fb, m0 + 64 * h, k0);
+                                }
+                            } else {
                                 if constexpr (PAIR)
-                                    tma_load_2d_pair(b_dst + j * 8192, &p.map_q, fb, n0 + 64 * j, k0);
+                                    tma_load_2d_pair(a_dst, &p.map_p, fb, k0, m0);
                                 else
-                                    tma_load_2d(b_dst + j * 8192, &p.map_q, fb, n0 + 64 * j, k0);
+                                    tma_load_2d(a_dst, &p.map_p, fb, k0, m0);
                             }
-                        } else {
-                            if constexpr (PAIR)
-                                tma_load_2d_pair(b_dst, &p.map_q, fb, k0, n0);
-                            else
-                                tma_load_2d(b_dst, &p.map_q, fb, k0, n0);
+                            if (p.q_3d) {
+                                if constexpr (PAIR)
+                                    tma_load_3d_pair(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
+                                else
+                                    tma_load_3d(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
+                            } else if (p.q_mn_major) {
+#pragma unroll
+                                for (int h = 0; h < TS::kBBoxes; ++h) {
+                                    if constexpr (PAIR)
+                                        tma_load_2d_pair(b_dst + h * 8192, &p.map_q, fb, n0 + 64 * h, k0);
+                                    else
+                                        tma_load_2d(b_dst + h * 8192, &p.map_q, fb, n0 + 64 * h, k0);
+                                }
+                            } else {
+                                if constexpr (PAIR)
+                                    tma_load_2d_pair(b_dst, &p.map_q, fb, k0, n0);
+                                else
+                                    tma_load_2d(b_dst, &p.map_q, fb, k0, n0);
+                            }
                         }
                     }
-                    if (++stage == STAGES) {
-                        stage = 0;
+                    g += n;
+                    if (++grp == GROUPS) {
+                        grp = 0;
                         phase ^= 1;
                     }
                 }
             }
             if (*abort_flag) {
                 // No TMA write may land after the CTA exits: wait for the last
-                // armed phase of every stage (the leader's barriers count the
+                // armed phase of every group (the leader's barriers count the
                 // bytes of both CTAs).
-                for (int s = 0; s < STAGES; ++s)
-                    if (armed & (1u << s)) drain_bar(smem_addr(&full[s]), (armed_parity >> s) & 1, w);
+                for (int q = 0; q < GROUPS; ++q)
+                    if (armed & (1u << q)) drain_bar(smem_addr(&full[q]), (armed_parity >> q) & 1, w);
             }
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer
-            int stage = 0;
+            constexpr int GROUPS = STAGES / kKPerStage;
+            int grp = 0;
             uint32_t phase = 0;
             bool ok = true;
             int i = 0;
@@ -580,26 +605,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 if (!wait_bar(smem_addr(&tempty[buf]), aph ^ 1, w, DEV_TIMEOUT_MMA + 1)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BN;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_bar(smem_addr(&full[stage]), phase, w, DEV_TIMEOUT_MMA + 2)) {
+                for (int kb = kb0; kb < kb1; kb += kKPerStage) {
+                    const int n = kb1 - kb < kKPerStage ? kb1 - kb : kKPerStage;
+                    if (!wait_bar(smem_addr(&full[grp]), phase, w, DEV_TIMEOUT_MMA + 2)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_lo = a_lo0 + (uint32_t)stage * (TS::kAStage >> 4);
-                    const uint32_t b_lo = b_lo0 + (uint32_t)stage * (TS::kBStage >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / kUmmaK; ++kk)
-                        mma_f16<CG>(d_tmem, smem_desc_join(a_lo + kk * a_kstep, d_hi),
-                                    smem_desc_join(b_lo + kk * b_kstep, d_hi), idesc,
-                                    (kb != kb0) || (kk != 0));
-                    // frees the stage (in both CTAs) once the MMAs have read it
+                    for (int j = 0; j < kKPerStage; ++j) {
+                        if (j >= n) break;
+                        const uint32_t slot = (uint32_t)(grp * kKPerStage + j);
+                        const uint32_t a_lo = a_lo0 + slot * (TS::kAStage >> 4);
+                        const uint32_t b_lo = b_lo0 + slot * (TS::kBStage >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / kUmmaK; ++kk)
+                            mma_f16<CG>(d_tmem, smem_desc_join(a_lo + kk * a_kstep, d_hi),
+                                        smem_desc_join(b_lo + kk * b_kstep, d_hi), idesc,
+                                        (kb + j != kb0) || (kk != 0));
+                    }
+                    // frees the group's slots (in both CTAs) once the MMAs have read them
                     if constexpr (PAIR)
-                        mma_commit_pair(smem_addr(&empty[stage]), 0x3);
+                        mma_commit_pair(smem_addr(&empty[grp]), 0x3);
                     else
-                        mma_commit(smem_addr(&empty[stage]));
-                    if (++stage == STAGES) {
-                        stage = 0;
+                        mma_commit(smem_addr(&empty[grp]));
+                    if (++grp == GROUPS) {
+                        grp = 0;
                         phase ^= 1;
                     }
                 }
