@@ -491,6 +491,9 @@ def main():
     ap.add_argument("--profile-others", action="store_true",
                     help="run each non-headline GEMM workload once after an L2 flush and exit "
                          "(one launch per workload, for ncu captures; prints the launch order)")
+    ap.add_argument("--profile-workload", default=None, metavar="KEY",
+                    help="run one GEMM workload three times and then once more, each call after "
+                         "an L2 flush, and exit (for a one-launch ncu capture: -s 3 -c 1)")
     ap.add_argument("--workload", default="fp16_4096", help="headline workload key")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-stream-k", action="store_true",
@@ -528,6 +531,21 @@ def main():
                               "steps": args.steps, "warmup": args.warmup,
                               "peak_gbs": float(peaks.get("hbm_gbs", 6800.0)),
                               "workloads": lines}), flush=True)
+        return
+
+    if args.profile_workload:
+        dp = DeviceProblem(tg, make_problem(specs[args.profile_workload]),
+                           stream_k=not args.no_stream_k)
+        for _ in range(4):
+            with torch.cuda.stream(stream):
+                flush.fill_(1)  # on the launching stream, so that every call starts cold
+            dp.call(stream)
+        torch.cuda.synchronize()
+        st, code = tg.tg_debug_status()
+        if st != tg.TG_OK:
+            raise RuntimeError(f"device watchdog fired: {code:#x}")
+        if rank == 0:
+            print(json.dumps({"workload": args.profile_workload, "tile": dp.config}), flush=True)
         return
 
     if args.profile_others:
