@@ -58,7 +58,8 @@ struct KBlocksPerStage {
 };
 constexpr int kUmmaK = 16;     // K per tcgen05.mma of kind::f16
 constexpr int kEpiWarps = 4;   // one epilogue warp per TMEM lane quadrant (8 measured no faster overall)
-constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, epilogue warps
+constexpr int kHelper0 = 2 + kEpiWarps;       // first of two warps that only help with a last item
+constexpr int kThreads = 64 + 32 * kEpiWarps + 64;  // producer, MMA, epilogue and helper warps
 constexpr int kStageBufs = 4;  // output staging buffers per epilogue warp
 
 template <int BN, bool PAIR>
@@ -76,7 +77,7 @@ struct TileShape {
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
     static constexpr int kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
                                    : 2 * BN <= 256 ? 256 : 512;
-    static constexpr int kSmemBytes = 1024 + kStages * kStage + kStaging + (2 * kStages + 5) * 8 + 16;
+    static constexpr int kSmemBytes = 1024 + kStages * kStage + kStaging + (2 * kStages + 7) * 8 + 16;
     static_assert(kStages >= 4, "too few pipeline stages");
     static_assert(kStages % 2 == 0, "ring slots come in whole barrier groups");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
@@ -436,9 +437,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* hsync = drain + 1;     // a last split tile's fix-up decision, for the helper warps
+    uint64_t* lastfull = hsync + 1;  // the worker's last accumulator is complete (one phase)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lastfull + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* sk_last = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    volatile int* sk_help = reinterpret_cast<volatile int*>(tmem_slot + 3);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -462,6 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             mbar_init(smem_addr(&tempty[b]), (PAIR ? 2 : 1) * kEpiWarps);  // one per epilogue warp
         }
         mbar_init(smem_addr(drain), 1);
+        mbar_init(smem_addr(hsync), 1);
+        mbar_init(smem_addr(lastfull), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -640,6 +646,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     mma_commit_pair(smem_addr(&tfull[buf]), 0x3);
                 else
                     mma_commit(smem_addr(&tfull[buf]));
+                // the last item's, again on a one-shot barrier for the helper
+                // warps (a parity wait on tfull could alias an earlier phase)
+                WorkIter peek = items;
+                int t2, a2, b2;
+                if (!peek.next(t2, a2, b2)) {
+                    if constexpr (PAIR)
+                        mma_commit_pair(smem_addr(lastfull), 0x3);
+                    else
+                        mma_commit(smem_addr(lastfull));
+                }
             }
             // Nothing may still write TMEM when it is released.
             if constexpr (PAIR)
@@ -648,23 +664,50 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 mma_commit(smem_addr(drain));
             drain_bar(smem_addr(drain), 0, w);
         }
-    } else {
-        // ---------------------------------------------------- epilogue
+    }
+
+    // -------------------------------------------------------- epilogue
+    // Warps 2 .. 1 + kEpiWarps finish every work item, one per TMEM lane
+    // quadrant.  Nothing overlaps the epilogue of a worker's last item, so
+    // that one is split with a second warp per quadrant (a "helper"): warps
+    // 0 and 1 once their producer / MMA role is done, and warps kHelper0 and
+    // kHelper0 + 1, which wait for it from the start.  A helper takes the
+    // second half of its quadrant's chunks and stages them in the operand
+    // ring, which no load or MMA touches once the last accumulator is
+    // complete.  Helpers meet the main warps at no named barrier: they learn
+    // a split tile's fix-up decision through the mbarrier `hsync`, with
+    // bounded waits, so an aborting CTA cannot strand them.
+    __syncwarp();  // the lanes of warps 0 and 1 wait for their role's lane 0
+    {
+        const bool helper = warp < 2 || warp >= kHelper0;
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         // the warps of a quadrant (kEpiWarps / 4 of them) split the tile's
         // 32-column chunks
         constexpr int kChunks = BN / 32;
         constexpr int kPerQuadrant = kEpiWarps / 4;
-        const int part = (warp - 2) / 4;
+        const int part = helper ? 0 : (warp - 2) / 4;
         const int c_begin = part * kChunks / kPerQuadrant;
         const int c_end = (part + 1) * kChunks / kPerQuadrant;
-        uint8_t* stage = staging + (warp - 2) * kStageBufs * 2048;  // this warp's output buffers
+        // this warp's output buffers
+        uint8_t* stage = helper ? sA + q * kStageBufs * 2048 : staging + (warp - 2) * kStageBufs * 2048;
         const uint64_t pol = AUX ? l2_policy_evict_first() : 0;     // residual lines are read once
         uint32_t chunks = 0;                           // output chunks stored so far
         int i = 0;
         WorkIter items(p, worker);
         int t, kb0, kb1;
         for (; items.next(t, kb0, kb1); ++i) {
+            bool last_item;
+            {
+                WorkIter peek = items;
+                int t2, a2, b2;
+                last_item = !peek.next(t2, a2, b2);
+            }
+            if (helper && !last_item) continue;
+            // this warp's chunks of a tile it finishes: all of its quadrant's,
+            // or for a last item the main warp's first half, the helper's second
+            const int mid = c_begin + (c_end - c_begin + 1) / 2;
+            const int cb = last_item && helper ? mid : c_begin;
+            const int ce = last_item && !helper ? mid : c_end;
             const int buf = i & 1;
             const uint32_t aph = (i >> 1) & 1;
             int tm, tn;
@@ -680,17 +723,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 // while the main loop still runs (one 64-byte run per lane and chunk).
                 if (whole && p.resid && !p.swap && rk < p.M) {
                     const uint16_t* rrow = static_cast<const uint16_t*>(p.resid) + (long long)rk * p.ldr;
-                    for (int c = c_begin + 1; c < c_end; ++c) {
+                    for (int c = cb + 1; c < ce; ++c) {
                         const int c0 = tn * BN + c * 32;
                         if (c0 < p.N) prefetch_global_l2(rrow + c0);
                     }
                 }
             }
-            bool cur_full = (AUX && whole) ? prefetch_aux(p, rk, tn * BN + c_begin * 32, cur, pol) : false;
+            bool cur_full = (AUX && whole && cb < ce) ? prefetch_aux(p, rk, tn * BN + cb * 32, cur, pol) : false;
             int ok = 1;
-            if (lane == 0) ok = wait_bar(smem_addr(&tfull[buf]), aph, w, DEV_TIMEOUT_EPILOGUE);
+            if (lane == 0) {
+                if (!helper) {
+                    ok = wait_bar(smem_addr(&tfull[buf]), aph, w, DEV_TIMEOUT_EPILOGUE);
+                } else {
+                    // A helper waits for the last item from the start, on a
+                    // one-shot barrier; its time limit covers every item
+                    // before it (each of which the main warps wait for within
+                    // one limit).
+                    Watch wt = w;
+                    wt.timeout = w.timeout * (long long)(i + 1);
+                    ok = wait_bar(smem_addr(lastfull), 0, wt, DEV_TIMEOUT_EPILOGUE + 3);
+                }
+            }
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            ok = epilogue_sync_and(ok);  // all four warps continue, or all stop
+            if (!helper) {
+                ok = epilogue_sync_and(ok);  // all main warps continue, or all stop
+            } else if (ok) {
+                drain_bar(smem_addr(lastfull), 0, w);  // complete: every lane observes it
+                fence_proxy_async_shared();  // the buffers last held TMA-written operands
+            }
             if (!ok) break;
             tc_fence_after();
             float row_scale = 1.0f, row_bias = 0.0f;
@@ -701,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
             const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
             const int row0 = tm * TS::kBM + (int)rank * 128 + q * 32;  // this warp's first row
-            if (c_begin == c_end) {
+            if (!helper && c_begin == c_end) {
                 // no columns for this warp (narrow tile): release the buffer at once
                 tc_fence_before();
                 __syncwarp();
@@ -724,47 +784,64 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 float* base = p.ws_partial + (size_t)wf * p.sk_cmax * slot +
                               (size_t)rank * 128 * BN + (size_t)(q * 32 + lane) * 4;
                 int* counter = p.ws_count + wf * 2 + rank;
-                // If every other part is already published this worker finishes
-                // the tile at once and never writes its own partial.
-                if (warp == 2 && lane == 0) {
-                    int seen;
-                    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(seen) : "l"(counter) : "memory");
-                    *sk_last = seen == contributors - 1;
-                }
-                const bool early_last = epilogue_sync_and(1) && *sk_last;
-#pragma unroll 1
-                for (int c = c_begin; c < c_end && !early_last; ++c) {
-                    uint32_t v[32];
-                    __syncwarp();
-                    tmem_ld_32x32b_x32(t_row + c * 32, v);
-                    tmem_wait_ld();
-                    float4* dst = reinterpret_cast<float4*>(base + (size_t)mine * slot) + c * 8 * 128;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        __stcg(dst + j * 128, make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
-                }
-                bool last = early_last;
-                if (!early_last) {
-                    // all four warps' partial stores happen-before the release below
-                    epilogue_sync_and(1);
+                bool last;
+                if (helper) {
+                    // the main warps' decision: finish the tile (1) or not (0)
+                    int got = 1;
+                    if (lane == 0) got = wait_bar(smem_addr(hsync), 0, w, DEV_TIMEOUT_EPILOGUE + 2);
+                    if (!__shfl_sync(0xffffffffu, got, 0)) break;
+                    drain_bar(smem_addr(hsync), 0, w);  // every lane observes it (acquire)
+                    last = *sk_help != 0;
+                    if (!last) continue;
+                } else {
+                    // If every other part is already published this worker finishes
+                    // the tile at once and never writes its own partial.
                     if (warp == 2 && lane == 0) {
-                        const bool l = atomic_add_release_gpu(counter, 1) == contributors - 1;
-                        if (l) fence_acquire_gpu();  // the other partials are visible to this CTA
-                        *sk_last = l;
+                        int seen;
+                        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(seen) : "l"(counter) : "memory");
+                        *sk_last = seen == contributors - 1;
                     }
-                    last = epilogue_sync_and(1) && *sk_last;
-                }
-                if (!last) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0 && c_begin != c_end) {
-                        if constexpr (PAIR)
-                            mbar_arrive_cluster(smem_addr(&tempty[buf]), 0);
-                        else
-                            mbar_arrive(smem_addr(&tempty[buf]));
+                    const bool early_last = epilogue_sync_and(1) && *sk_last;
+#pragma unroll 1
+                    for (int c = c_begin; c < c_end && !early_last; ++c) {
+                        uint32_t v[32];
+                        __syncwarp();
+                        tmem_ld_32x32b_x32(t_row + c * 32, v);
+                        tmem_wait_ld();
+                        float4* dst = reinterpret_cast<float4*>(base + (size_t)mine * slot) + c * 8 * 128;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            __stcg(dst + j * 128, make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                        __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
                     }
-                    continue;
+                    last = early_last;
+                    if (!early_last) {
+                        // all four warps' partial stores happen-before the release below
+                        epilogue_sync_and(1);
+                        if (warp == 2 && lane == 0) {
+                            const bool l = atomic_add_release_gpu(counter, 1) == contributors - 1;
+                            if (l) fence_acquire_gpu();  // the other partials are visible to this CTA
+                            *sk_last = l;
+                        }
+                        last = epilogue_sync_and(1) && *sk_last;
+                    }
+                    if (last_item && warp == 2 && lane == 0) {
+                        // tell the helpers (release: with the acquire above, the
+                        // other partials are visible to them too)
+                        *sk_help = last ? 1 : 0;
+                        mbar_arrive(smem_addr(hsync));
+                    }
+                    if (!last) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0 && c_begin != c_end) {
+                            if constexpr (PAIR)
+                                mbar_arrive_cluster(smem_addr(&tempty[buf]), 0);
+                            else
+                                mbar_arrive(smem_addr(&tempty[buf]));
+                        }
+                        continue;
+                    }
                 }
                 // last to arrive: every other partial is published; add them
                 // all in K order (own part from TMEM) and finish the tile.  The
@@ -772,28 +849,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 // finished (two contributors is the common case).
                 const int other = contributors == 2 ? 1 - mine : -1;
                 float4 pre[8];
-                if (other >= 0) {
+                if (other >= 0 && cb < ce) {
                     const float4* src = reinterpret_cast<const float4*>(base + (size_t)other * slot) +
-                                        c_begin * 8 * 128;
+                                        cb * 8 * 128;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) pre[j] = __ldcg(src + j * 128);
                 }
 #pragma unroll 1
-                for (int c = c_begin; c < c_end; ++c) {
+                for (int c = cb; c < ce; ++c) {
                     uint32_t v[32];
                     __syncwarp();
                     tmem_ld_32x32b_x32(t_row + c * 32, v);
                     float4 cur4[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) cur4[j] = pre[j];
-                    if (other >= 0 && c + 1 < c_end) {
+                    if (other >= 0 && c + 1 < ce) {
                         const float4* src = reinterpret_cast<const float4*>(base + (size_t)other * slot) +
                                             (c + 1) * 8 * 128;
 #pragma unroll
                         for (int j = 0; j < 8; ++j) pre[j] = __ldcg(src + j * 128);
                     }
                     tmem_wait_ld();
-                    if (c == c_end - 1) {
+                    if (c == ce - 1 && !helper) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) {
@@ -845,12 +922,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 continue;
             }
 #pragma unroll 1
-            for (int c = c_begin; c < c_end; ++c) {
+            for (int c = cb; c < ce; ++c) {
                 uint32_t v[32];
                 __syncwarp();
                 tmem_ld_32x32b_x32(t_row + c * 32, v);
                 tmem_wait_ld();
-                if (c == c_end - 1) {
+                if (c == ce - 1 && !helper) {
                     // every column of this buffer is in registers: release it
                     tc_fence_before();
                     __syncwarp();
@@ -870,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
                 if constexpr (AUX) {
                     bool nxt_full = false;
-                    if (c + 1 < c_end)
+                    if (c + 1 < ce)
                         nxt_full = prefetch_aux(p, rk, tn * BN + (c + 1) * 32, nxt, pol);
                     finish_chunk(p, stage, chunks, lane, rk, row0, tn * BN + c * 32, y, row_scale,
                                  cur_full ? &cur : nullptr);
