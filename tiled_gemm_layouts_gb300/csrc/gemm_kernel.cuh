@@ -147,19 +147,8 @@ __device__ __forceinline__ uint16_t from_f32(float x, int bf16) {
     return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
 }
 
-// Two 16-bit values packed in a word -> two floats / two floats -> one word
-// with round-to-nearest-even, for a dtype fixed at compile time.
-template <bool BF>
-__device__ __forceinline__ float2 unpack2(uint32_t w) {
-    if constexpr (BF) {
-        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-    } else {
-        __half2 h;
-        *reinterpret_cast<uint32_t*>(&h) = w;
-        return __half22float2(h);
-    }
-}
-
+// Two floats -> one word of two 16-bit values with round-to-nearest-even, for
+// a dtype fixed at compile time.
 template <bool BF>
 __device__ __forceinline__ uint32_t pack2t(float a, float b) {
     uint32_t w;
@@ -173,18 +162,26 @@ __device__ __forceinline__ uint32_t pack2t(float a, float b) {
     return w;
 }
 
-// y[0], y[1] += x0, x1 as one packed fp32x2 add (round to nearest): half
-// the arithmetic instructions of the epilogue warps, which share issue slots
-// with the single-thread producer and MMA loops.
-__device__ __forceinline__ void add2(float* y, float x0, float x1) {
-    unsigned long long a, b;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(y[0]), "f"(y[1]));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(x0), "f"(x1));
-    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(b));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(y[0]), "=f"(y[1]) : "l"(a));
+// y[0], y[1] += the two 16-bit values of w (low half first).  Each is added
+// by one mixed-precision add: the 16-bit operand is widened exactly and the
+// fp32 sum rounded once to nearest, the same result as converting first,
+// without the conversion instructions.
+template <bool BF>
+__device__ __forceinline__ void add2_wide(float* y, uint32_t w) {
+    if constexpr (BF)
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+            : "+f"(y[0]), "+f"(y[1])
+            : "r"(w));
+    else
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+            : "+f"(y[0]), "+f"(y[1])
+            : "r"(w));
 }
 
-// y[0], y[1] *= s as one packed fp32x2 multiply (round to nearest).
+// y[0], y[1] *= s as one packed fp32x2 multiply (round to nearest): half the
+// multiply instructions of the epilogue warps.
 __device__ __forceinline__ void mul2(float* y, float s) {
     unsigned long long a, b;
     asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(y[0]), "f"(y[1]));
@@ -195,12 +192,10 @@ __device__ __forceinline__ void mul2(float* y, float s) {
 
 template <bool BF>
 __device__ __forceinline__ void add8(const uint4& u, float* y) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = unpack2<BF>(w[i]);
-        add2(y + 2 * i, f.x, f.y);
-    }
+    add2_wide<BF>(y, u.x);
+    add2_wide<BF>(y + 2, u.y);
+    add2_wide<BF>(y + 4, u.z);
+    add2_wide<BF>(y + 6, u.w);
 }
 
 // Residual and bias values of one full 32-column run of row m, loaded ahead
@@ -715,20 +710,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const int rk = tm * TS::kBM + (int)rank * 128 + q * 32 + lane;
             const bool whole = !SK || (kb0 == 0 && kb1 == p.num_kb);
             // operands of the first run do not depend on the accumulator:
-            // fetch them while the main loop still runs
+            // fetch them while the main loop still runs.  (Moving the later
+            // runs' residual rows into L2 here as well measured 1.2 % slower
+            // on the fused GEMM: they evict operand lines.)
             Aux cur, nxt;
-            if constexpr (AUX) {
-                // The residual rows of this warp's chunks are read only after
-                // the accumulator is ready: start moving them into L2 now,
-                // while the main loop still runs (one 64-byte run per lane and chunk).
-                if (whole && p.resid && !p.swap && rk < p.M) {
-                    const uint16_t* rrow = static_cast<const uint16_t*>(p.resid) + (long long)rk * p.ldr;
-                    for (int c = cb + 1; c < ce; ++c) {
-                        const int c0 = tn * BN + c * 32;
-                        if (c0 < p.N) prefetch_global_l2(rrow + c0);
-                    }
-                }
-            }
             bool cur_full = (AUX && whole && cb < ce) ? prefetch_aux(p, rk, tn * BN + cb * 32, cur, pol) : false;
             int ok = 1;
             if (lane == 0) {

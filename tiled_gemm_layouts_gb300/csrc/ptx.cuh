@@ -172,11 +172,6 @@ __device__ __forceinline__ void bulk_wait_group() {
 }
 
 // Orders generic-proxy shared-memory writes before later async-proxy reads.
-// Hint: bring the cache line holding p into L2 (no register result).
-__device__ __forceinline__ void prefetch_global_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
