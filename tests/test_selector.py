@@ -130,19 +130,21 @@ def test_stream_k_invariants(tg, seed):
 
 def simulate_items(workers, dp_tiles, sk_tiles, kb):
     """The kernel's work split, restated: whole tiles w, w+workers, ... below
-    dp_tiles, then equal contiguous ranges of the sk_tiles*kb iterations."""
+    dp_tiles and equal contiguous ranges of the sk_tiles*kb iterations, in the
+    kernel's order: every whole tile but the last, the range, the last one."""
     iters = sk_tiles * kb
     items = {}
     for w in range(workers):
-        out = [(t, 0, kb) for t in range(w, dp_tiles, workers)]
+        whole = [(t, 0, kb) for t in range(w, dp_tiles, workers)]
+        pieces = []
         it, end = iters * w // workers, iters * (w + 1) // workers
         while it < end:
             ts = it // kb
             k0 = it - ts * kb
             k1 = min(kb, k0 + (end - it))
-            out.append((dp_tiles + ts, k0, k1))
+            pieces.append((dp_tiles + ts, k0, k1))
             it += k1 - k0
-        items[w] = out
+        items[w] = whole[:-1] + pieces + whole[-1:]
     return items
 
 
@@ -166,6 +168,9 @@ def test_stream_k_schedule_covers_every_k_block_once(tg, seed):
                 seen[(t, k)] = w
             owners.setdefault(t, []).append(w)
     assert len(seen) == c["tiles"] * kb
+    for w, its in items.items():  # a worker holding whole tiles ends on one
+        if any(k1 - k0 == kb and t < dp for t, k0, k1 in its):
+            assert its[-1][0] < dp
     first_owners = set()
     for t, ws in owners.items():
         assert ws == sorted(ws) and ws == list(range(ws[0], ws[0] + len(ws)))

@@ -353,19 +353,26 @@ __device__ __forceinline__ void epilogue_swap(const GemmParams& p, int rk, int c
     }
 }
 
-// The work items of one persistent worker: its whole tiles first (worker w
-// takes tiles w, w + workers, ... below dp_tiles), then its contiguous range
-// of stream-K iterations, cut at tile boundaries into (tile, k-block range).
+// The work items of one persistent worker.  Its whole tiles are w, w +
+// workers, ... below dp_tiles; its stream-K iterations are one contiguous
+// range, cut at tile boundaries into (tile, k-block range) pieces.  Order: all
+// whole tiles but the last, then the range, then the last whole tile.  So a
+// worker ends on a whole tile, whose epilogue the helper warps halve, and the
+// fix-ups of split tiles run beside that tile's main loop.  (With the range
+// last, the worker finishing a split tile did so in its final item, queued
+// behind the previous tile's epilogue: 4096^3 measured 1-2 % slower.)
 struct WorkIter {
-    int workers, dp_tiles, num_kb, dp_next;
+    int workers, dp_tiles, num_kb, dp_next, dp_left;
     long long it, it_end;
 
     __device__ __forceinline__ WorkIter(const GemmParams& p, int worker)
         : workers(p.workers), dp_tiles(p.dp_tiles), num_kb(p.num_kb), dp_next(worker),
+          dp_left(worker < p.dp_tiles ? (p.dp_tiles - worker + p.workers - 1) / p.workers : 0),
           it(p.sk_iters * worker / p.workers), it_end(p.sk_iters * (worker + 1) / p.workers) {}
 
     __device__ __forceinline__ bool next(int& tile, int& kb0, int& kb1) {
-        if (dp_next < dp_tiles) {
+        if (dp_left > 1 || (dp_left == 1 && it >= it_end)) {
+            --dp_left;
             tile = dp_next;
             kb0 = 0;
             kb1 = num_kb;
