@@ -190,6 +190,25 @@ __device__ __forceinline__ void mul2(float* y, float s) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(y[0]), "=f"(y[1]) : "l"(a));
 }
 
+// y[0], y[1] += x0, x1 as one packed fp32x2 add (round to nearest).
+__device__ __forceinline__ void add2(float* y, float x0, float x1) {
+    unsigned long long a, b;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(y[0]), "f"(y[1]));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(x0), "f"(x1));
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(b));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(y[0]), "=f"(y[1]) : "l"(a));
+}
+
+// v[i] for a run-time i without indexing the array (which would put it in
+// local memory): N selects, N <= 8.
+template <int N>
+__device__ __forceinline__ float pick(const float (&v)[N], int i) {
+    float r = 0.0f;
+#pragma unroll
+    for (int k = 0; k < N; ++k) r = k == i ? v[k] : r;
+    return r;
+}
+
 template <bool BF>
 __device__ __forceinline__ void add8(const uint4& u, float* y) {
     add2_wide<BF>(y, u.x);
@@ -198,15 +217,16 @@ __device__ __forceinline__ void add8(const uint4& u, float* y) {
     add2_wide<BF>(y + 6, u.w);
 }
 
-// Residual and bias values of one full 32-column run of row m, loaded ahead
-// of the accumulator so that their latency overlaps the TMEM read.
+// Residual values of one full 32-column run of row m, loaded one run ahead
+// (and before the accumulator is ready) so that their latency overlaps the
+// work on the run before.
 struct Aux {
     uint4 r[4];
-    uint4 b[4];
 };
 
-// Issues the loads for the run C(m, c0 .. c0+31) if it is full and inside C;
-// returns whether it is (otherwise the chunk takes the masked scalar path).
+// Issues the residual loads for the run C(m, c0 .. c0+31) if it is full and
+// inside C; returns whether it is (otherwise the chunk takes the masked
+// scalar path).
 // Residual lines are read exactly once: `pol` marks them first to leave L2,
 // so they do not push operand panels out (measured +0.3 % on the fused GEMM).
 __device__ __forceinline__ bool prefetch_aux(const GemmParams& p, int m, int c0, Aux& a,
@@ -218,38 +238,28 @@ __device__ __forceinline__ bool prefetch_aux(const GemmParams& p, int m, int c0,
 #pragma unroll
         for (int v = 0; v < 4; ++v) a.r[v] = ld_nc_hint(r + v, pol);
     }
-    if (p.bias_n) {
-        const uint4* b = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.bias_n) + c0);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) a.b[v] = __ldg(b + v);
-    }
     return true;
 }
 
 // Epilogue arithmetic for the run C(m, c0 .. c0+31) held in y[], in fp32:
-// scale, bias, ReLU, residual.  `a` holds the prefetched bias/residual of a
-// full in-bounds run; otherwise (edge runs) they are loaded here with
-// per-element masks.  Values outside C are computed but never stored.
+// scale, bias, ReLU, residual.  Called by all 32 lanes of a warp together
+// (lane = row): lane j holds in `bias_lane` the bias of column c0 + j (0
+// outside C), which shuffles hand to every row.  `a` holds the prefetched
+// residual of a full in-bounds run; otherwise (edge runs) it is loaded here
+// with per-element masks.  Values outside C are computed but never stored.
 template <bool BF>
 __device__ __forceinline__ void epilogue_math(const GemmParams& p, int m, int c0, float (&y)[32],
-                                              float row_scale, const Aux* a) {
+                                              float row_scale, float bias_lane, const Aux* a) {
     const bool inside = m < p.M && c0 < p.N;
     const bool full = inside && c0 + 32 <= p.N;
     if (p.scale_m) {
 #pragma unroll
         for (int j = 0; j < 32; j += 2) mul2(y + j, row_scale);
     }
-    if (p.bias_n && inside) {
-        const uint16_t* b = static_cast<const uint16_t*>(p.bias_n) + c0;
-        if (full) {
+    if (p.bias_n) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-                add8<BF>(a ? a->b[v] : __ldg(reinterpret_cast<const uint4*>(b) + v), y + 8 * v);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (c0 + j < p.N) y[j] += to_f32(b[j], BF);
-        }
+        for (int j = 0; j < 32; j += 2)
+            add2(y + j, __shfl_sync(0xffffffffu, bias_lane, j), __shfl_sync(0xffffffffu, bias_lane, j + 1));
     }
     if (p.relu) {
 #pragma unroll
@@ -321,12 +331,12 @@ __device__ __forceinline__ void store_chunk(const GemmParams& p, uint8_t* stage,
 // resolved once per chunk (instead of per element).
 __device__ __forceinline__ void finish_chunk(const GemmParams& p, uint8_t* stage, uint32_t& count,
                                              int lane, int rk, int row0, int c0, float (&y)[32],
-                                             float row_scale, const Aux* a) {
+                                             float row_scale, float bias_lane, const Aux* a) {
     if (p.bf16) {
-        epilogue_math<true>(p, rk, c0, y, row_scale, a);
+        epilogue_math<true>(p, rk, c0, y, row_scale, bias_lane, a);
         store_chunk<true>(p, stage, count, lane, row0, c0, y);
     } else {
-        epilogue_math<false>(p, rk, c0, y, row_scale, a);
+        epilogue_math<false>(p, rk, c0, y, row_scale, bias_lane, a);
         store_chunk<false>(p, stage, count, lane, row0, c0, y);
     }
 }
@@ -415,8 +425,9 @@ __device__ __forceinline__ int epilogue_sync_and(int v) {
     return (int)out;
 }
 
-// AUX = true: the epilogue reads a bias and/or residual; their loads are
-// issued one 32-column run ahead (and before the accumulator is ready).
+// AUX = true: the epilogue reads a bias and/or residual: the bias once per
+// tile, the residual one 32-column run ahead (both issued before the
+// accumulator is ready).
 // AUX = false keeps the plain epilogue lean.
 // SK = true: the launch deals tail tiles out in K-ranges (the stream-K code is
 // compiled only into these instantiations; whole-tile kernels stay lean).
@@ -716,10 +727,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tile_coords(p, t, tm, tn);
             const int rk = tm * TS::kBM + (int)rank * 128 + q * 32 + lane;
             const bool whole = !SK || (kb0 == 0 && kb1 == p.num_kb);
-            // operands of the first run do not depend on the accumulator:
-            // fetch them while the main loop still runs.  (Moving the later
-            // runs' residual rows into L2 here as well measured 1.2 % slower
-            // on the fused GEMM: they evict operand lines.)
+            // Lane j's bias of column j of each of this warp's chunks, loaded
+            // once per tile before the accumulator wait; a chunk hands them
+            // to its rows by shuffles.  (A broadcast load of each chunk's 32
+            // values, one chunk ahead, sat in the epilogue's dependent chain:
+            // 4096 x 3136 x 1024 with a bias ran 10 % slower than without.)
+            float bcol[kChunks];
+#pragma unroll
+            for (int k = 0; k < kChunks; ++k) bcol[k] = 0.0f;
+            if constexpr (AUX) {
+                if (p.bias_n && !p.swap) {
+                    const uint16_t* bv = static_cast<const uint16_t*>(p.bias_n);
+#pragma unroll
+                    for (int k = 0; k < kChunks; ++k) {
+                        const int n = tn * BN + k * 32 + lane;
+                        if (k >= cb && k < ce && n < p.N) bcol[k] = to_f32(bv[n], p.bf16);
+                    }
+                }
+            }
+            // the residual of the first run does not depend on the
+            // accumulator: fetch it while the main loop still runs.  (Moving
+            // the later runs' residual rows into L2 here as well measured
+            // 1.2 % slower on the fused GEMM: they evict operand lines.)
             Aux cur, nxt;
             bool cur_full = (AUX && whole && cb < ce) ? prefetch_aux(p, rk, tn * BN + cb * 32, cur, pol) : false;
             int ok = 1;
@@ -907,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         epilogue_swap(p, rk, tn * BN + c * 32, y, row_bias);
                     } else {
                         finish_chunk(p, stage, chunks, lane, rk, row0, tn * BN + c * 32, y, row_scale,
-                                     nullptr);
+                                     pick(bcol, c), nullptr);
                     }
                 }
                 if (warp == 2 && lane == 0) *counter = 0;  // ready for the next call
@@ -942,12 +971,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     if (c + 1 < ce)
                         nxt_full = prefetch_aux(p, rk, tn * BN + (c + 1) * 32, nxt, pol);
                     finish_chunk(p, stage, chunks, lane, rk, row0, tn * BN + c * 32, y, row_scale,
-                                 cur_full ? &cur : nullptr);
+                                 pick(bcol, c), cur_full ? &cur : nullptr);
                     cur = nxt;
                     cur_full = nxt_full;
                 } else {
                     finish_chunk(p, stage, chunks, lane, rk, row0, tn * BN + c * 32, y, row_scale,
-                                 nullptr);
+                                 0.0f, nullptr);
                 }
             }
         }
