@@ -36,7 +36,7 @@ size_t region(int64_t rows, int64_t width) {  // dense rows x up8(width) 16-bit 
 
 // Rows of C per pipelined block: whole 256-row tile pairs, about four blocks.
 // Measured at 4096^3 on GB300 (host link about 208 GB/s in, 192 GB/s out,
-// about 250 GB/s both ways at once): 1024-row blocks 0.46 ms, 512: 0.47,
+// about 340 GB/s both ways at once): 1024-row blocks 0.46 ms, 512: 0.47,
 // 256: 0.54, one block (no overlap): 0.60.  No C leaves before all of B and
 // the first block of A have arrived, and the last block's GEMM and copy-out
 // stay exposed: fewer, larger blocks lose overlap; more, smaller ones run
