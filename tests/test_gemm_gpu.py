@@ -123,6 +123,18 @@ def test_every_tile_configuration(tg, force, permA, permB, M, N, K):
     full_check(tg, p, force=force, what=force)
 
 
+@pytest.mark.parametrize("force", ["pair=1,bn=224,swap=0", "pair=0,bn=224,swap=0", "pair=1,bn=256,swap=0",
+                                   "pair=1,bn=224,grid=4,swap=0"])
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_column_bias_across_tiles(tg, force, dtype):
+    # Each lane loads its column's bias once per tile; a chunk broadcasts the
+    # values to its rows.  N spans several tile columns (odd ones included)
+    # and ends mid-chunk; grid=4 gives every worker several tiles, so the
+    # main and helper warps split only the last one.
+    p = synthetic.gemm_problem(520, 712, 200, dtype, 71, bias=True)
+    full_check(tg, p, force=force, what=f"bias {force}")
+
+
 def test_swap_selected_for_small_M(tg):
     cfg = tg.parse_config(tg.tg_query_config(32, 16384, 16384, BF16))
     assert cfg["swap"] == 1

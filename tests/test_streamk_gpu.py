@@ -53,6 +53,8 @@ CASES = [
     (520, 300, 2000, F16, "pair=0,bn=256,grid=8,sk=1", {}),            # no whole-tile waves at all
     (32, 1000, 2048, BF16, "pair=0,bn=32,swap=1,grid=16,sk=1", dict(scale=True)),
     (200, 900, 3000, F16, "pair=0,bn=64,grid=12,sk=1", dict(bias=True)),
+    # column bias held per lane, in 224-wide tiles over several tile columns (odd ones too)
+    (1000, 712, 2048, F16, "pair=1,bn=224,grid=10,sk=1", dict(bias=True)),
 ]
 
 
