@@ -135,6 +135,19 @@ def test_column_bias_across_tiles(tg, force, dtype):
     full_check(tg, p, force=force, what=f"bias {force}")
 
 
+@pytest.mark.parametrize("force", ["pair=1,bn=256,swap=0", "pair=0,bn=128,swap=0", "pair=0,bn=192,swap=0",
+                                   "pair=0,bn=256,swap=0", "pair=1,bn=256,grid=4,swap=0"])
+@pytest.mark.parametrize("K", [384, 448])
+def test_two_kblock_boxes(tg, force, K):
+    # Whole-tile kernels fill two ring slots per barrier transaction; with A
+    # K-major, B N-major (N a multiple of 64) and K a multiple of 64, each
+    # operand's pair of K-blocks arrives as one 3-D (A) or 4-D (B) box.  K =
+    # 448 leaves an odd last K-block, which takes the one-block boxes; M is
+    # ragged (rows past M read as zeros).
+    p = synthetic.gemm_problem(600, 704, K, F16, 81, bias=True, residual=True)
+    full_check(tg, p, force=force, what=f"2k {force}")
+
+
 def test_swap_selected_for_small_M(tg):
     cfg = tg.parse_config(tg.tg_query_config(32, 16384, 16384, BF16))
     assert cfg["swap"] == 1

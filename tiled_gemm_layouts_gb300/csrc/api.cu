@@ -258,6 +258,46 @@ bool encode_mn_atoms(CUtensorMap* map, int dtype, const void* base, int64_t rows
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Two consecutive K-blocks of an operand as one box, for kernels that fill
+// two ring slots per barrier transaction: the box lands as the two slots'
+// stages back to back, so the pair takes one TMA instruction per operand
+// instead of two (each instruction costs TMA throughput).  Only for K a
+// multiple of 64: the K-block dimension spans whole blocks.
+// K-major operand (`rows` x K, K contiguous): dims {64, rows, K / 64},
+// strides {ld, 64} elements, box {64, box_rows, 2}.
+bool encode_k_pairs(CUtensorMap* map, int dtype, const void* base, int64_t rows, int64_t k,
+                    int64_t ld, uint32_t box_rows) {
+    if (k % 64 != 0 || k < 128) return false;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(k / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
+    const cuuint32_t box[3] = {64, box_rows, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        dtype == TG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// MN-major operand whose stage is `atoms` 64-wide atoms (as encode_mn_atoms),
+// two K-blocks per box: dims {64, 64, rows / 64, K / 64}, strides
+// {ld, 64, 64 * ld} elements, box {64, 64, atoms, 2}.
+bool encode_mn_atom_pairs(CUtensorMap* map, int dtype, const void* base, int64_t rows, int64_t k,
+                          int64_t ld, uint32_t atoms) {
+    if (rows % 64 != 0 || atoms < 2 || atoms > 4 || k % 64 != 0 || k < 128) return false;
+    const cuuint64_t dims[4] = {64, 64, (cuuint64_t)(rows / 64), (cuuint64_t)(k / 64)};
+    const cuuint64_t strides[3] = {(cuuint64_t)ld * 2, 128, (cuuint64_t)ld * 2 * 64};
+    const cuuint32_t box[4] = {64, 64, atoms, 2};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType dt =
+        dtype == TG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return g_encode(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 uint32_t make_idesc(int dtype, bool p_mn, bool q_mn, int n, int m) {
     const uint32_t fmt = dtype == TG_BF16 ? 1u : 0u;
     return (1u << 4)                   // accumulator format: fp32
@@ -420,6 +460,11 @@ int gemm_impl(const Args& user, void* workspace, size_t ws_bytes, cudaStream_t s
              encode_mn_atoms(&p.map_q, a.dtype, q_base, p.Nk, a.K, q_ld, (uint32_t)(q_box / 64));
     ok = (p.p_3d || encode_operand(&p.map_p, a.dtype, p_base, p.Mk, a.K, p_ld, p_mn, 128)) &&
          (p.q_3d || encode_operand(&p.map_q, a.dtype, q_base, p.Nk, a.K, q_ld, q_mn, q_box));
+    // two-K-block boxes for kernels that pair ring slots (whole-tile kernels)
+    const bool pairs_slots = cfg.sk_tiles == 0;
+    p.p_2k = pairs_slots && !p_mn && encode_k_pairs(&p.map_p2, a.dtype, p_base, p.Mk, a.K, p_ld, 128);
+    p.q_2k = p.p_2k && p.q_3d &&
+             encode_mn_atom_pairs(&p.map_q2, a.dtype, q_base, p.Nk, a.K, q_ld, (uint32_t)(q_box / 64));
     // C for the epilogue's tensor stores: 32 x 32 chunks, rows of 64 bytes.
     // A tensor store bounds the innermost dimension in 16-byte units, so the
     // map stops at N rounded down to 8 columns; the kernel stores the rest

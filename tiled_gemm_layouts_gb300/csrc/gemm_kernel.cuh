@@ -512,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const uint32_t a_bytes = TS::kAStage;
             const uint32_t b_bytes = p.q_mn_major ? (uint32_t)TS::kBStage : (uint32_t)TS::kBNC * 128u;
             const uint32_t stage_tx = (a_bytes + b_bytes) * (PAIR ? 2u : 1u);
+            const bool both_2k = p.p_2k && p.q_2k;  // both operands have two-K-block maps
             WorkIter items(p, worker);
             int t, kb0, kb1;
             while (ok && items.next(t, kb0, kb1)) {
@@ -533,50 +534,63 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                             armed_parity = (armed_parity & ~(1u << grp)) | (phase << grp);
                         }
                         const uint32_t fb = PAIR ? mapa_shared(fb_local, 0) : fb_local;
-#pragma unroll
-                        for (int j = 0; j < kKPerStage; ++j) {
-                            if (j >= n) break;
-                            const int slot = grp * kKPerStage + j;
-                            const uint32_t a_dst = smem_addr(sA + slot * TS::kAStage);
-                            const uint32_t b_dst = smem_addr(sB + slot * TS::kBStage);
-                            const int k0 = (kb + j) * kBK;
-                            if (p.p_3d) {
-                                if constexpr (PAIR)
-                                    tma_load_3d_pair(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
-                                else
-                                    tma_load_3d(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
-                            } else if (p.p_mn_major) {
-#pragma unroll
-                                for (int h = 0; h < 2; ++h) {
-                                    if constexpr (PAIR)
-                                        tma_load_2d_pair(a_dst + h * 8192, &p.map_p, fb, m0 + 64 * h, k0);
-                                    else
-                                        tma_load_2d(a_dst + h * 8192, &p.map_p, fb, m0 + 64 * h, k0);
-                                }
+                        if (kKPerStage == 2 && n == 2 && both_2k) {
+                            // both K-blocks of each operand as one box
+                            const uint32_t a_dst = smem_addr(sA + grp * kKPerStage * TS::kAStage);
+                            const uint32_t b_dst = smem_addr(sB + grp * kKPerStage * TS::kBStage);
+                            if constexpr (PAIR) {
+                                tma_load_3d_pair(a_dst, &p.map_p2, fb, 0, m0, kb);
+                                tma_load_4d_pair(b_dst, &p.map_q2, fb, 0, 0, n0 >> 6, kb);
                             } else {
-                                if constexpr (PAIR)
-                                    tma_load_2d_pair(a_dst, &p.map_p, fb, k0, m0);
-                                else
-                                    tma_load_2d(a_dst, &p.map_p, fb, k0, m0);
+                                tma_load_3d(a_dst, &p.map_p2, fb, 0, m0, kb);
+                                tma_load_4d(b_dst, &p.map_q2, fb, 0, 0, n0 >> 6, kb);
                             }
-                            if (p.q_3d) {
-                                if constexpr (PAIR)
-                                    tma_load_3d_pair(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
-                                else
-                                    tma_load_3d(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
-                            } else if (p.q_mn_major) {
+                        } else {
 #pragma unroll
-                                for (int h = 0; h < TS::kBBoxes; ++h) {
+                            for (int j = 0; j < kKPerStage; ++j) {
+                                if (j >= n) break;
+                                const int slot = grp * kKPerStage + j;
+                                const uint32_t a_dst = smem_addr(sA + slot * TS::kAStage);
+                                const uint32_t b_dst = smem_addr(sB + slot * TS::kBStage);
+                                const int k0 = (kb + j) * kBK;
+                                if (p.p_3d) {
                                     if constexpr (PAIR)
-                                        tma_load_2d_pair(b_dst + h * 8192, &p.map_q, fb, n0 + 64 * h, k0);
+                                        tma_load_3d_pair(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
                                     else
-                                        tma_load_2d(b_dst + h * 8192, &p.map_q, fb, n0 + 64 * h, k0);
+                                        tma_load_3d(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
+                                } else if (p.p_mn_major) {
+#pragma unroll
+                                    for (int h = 0; h < 2; ++h) {
+                                        if constexpr (PAIR)
+                                            tma_load_2d_pair(a_dst + h * 8192, &p.map_p, fb, m0 + 64 * h, k0);
+                                        else
+                                            tma_load_2d(a_dst + h * 8192, &p.map_p, fb, m0 + 64 * h, k0);
+                                    }
+                                } else {
+                                    if constexpr (PAIR)
+                                        tma_load_2d_pair(a_dst, &p.map_p, fb, k0, m0);
+                                    else
+                                        tma_load_2d(a_dst, &p.map_p, fb, k0, m0);
                                 }
-                            } else {
-                                if constexpr (PAIR)
-                                    tma_load_2d_pair(b_dst, &p.map_q, fb, k0, n0);
-                                else
-                                    tma_load_2d(b_dst, &p.map_q, fb, k0, n0);
+                                if (p.q_3d) {
+                                    if constexpr (PAIR)
+                                        tma_load_3d_pair(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
+                                    else
+                                        tma_load_3d(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
+                                } else if (p.q_mn_major) {
+#pragma unroll
+                                    for (int h = 0; h < TS::kBBoxes; ++h) {
+                                        if constexpr (PAIR)
+                                            tma_load_2d_pair(b_dst + h * 8192, &p.map_q, fb, n0 + 64 * h, k0);
+                                        else
+                                            tma_load_2d(b_dst + h * 8192, &p.map_q, fb, n0 + 64 * h, k0);
+                                    }
+                                } else {
+                                    if constexpr (PAIR)
+                                        tma_load_2d_pair(b_dst, &p.map_q, fb, k0, n0);
+                                    else
+                                        tma_load_2d(b_dst, &p.map_q, fb, k0, n0);
+                                }
                             }
                         }
                     }

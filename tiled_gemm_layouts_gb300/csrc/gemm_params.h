@@ -23,6 +23,10 @@ struct alignas(128) GemmParams {
     CUtensorMap map_p;   // P operand: K-major box {64, BM} or MN-major box {64, 64}
     CUtensorMap map_q;   // Q operand: K-major box {64, BN} or MN-major box {64, 64}
     CUtensorMap map_c;   // C for tensor stores: box {32 columns, 32 rows}, 64-byte swizzle
+    // Two consecutive K-blocks of an operand as one box (valid when p_2k / q_2k):
+    // P K-major {64, BM rows, 2 blocks}; Q MN-major {64, 64, atoms, 2 blocks}
+    CUtensorMap map_p2;
+    CUtensorMap map_q2;
     int Mk, Nk, K;       // kernel-side problem (after the optional swap)
     int num_kb;          // ceil(K / 64)
     int tiles_m, tiles_n, num_tiles;
@@ -31,6 +35,7 @@ struct alignas(128) GemmParams {
     int p_mn_major;      // 1: P tile stored MN-major in shared memory
     int q_mn_major;
     int p_3d, q_3d;      // 1: an MN-major stage arrives as one 3-D box (all its 64-wide atoms)
+    int p_2k, q_2k;      // 1: map_p2 / map_q2 load two K-blocks (K a multiple of 64)
     int swap;            // 1: D is C^T
     int bf16;            // element type of every operand: 0 fp16, 1 bf16
     // epilogue, in C's (m, n) coordinates
