@@ -402,6 +402,12 @@ struct WorkIter {
     }
 };
 
+// Compile-time role of a producer thread.
+template <int V>
+struct RoleTag {
+    static constexpr int value = V;
+};
+
 // Worker whose stream-K range holds iteration `it`.
 __device__ __forceinline__ int sk_owner(const GemmParams& p, long long it) {
     int w = (int)(it * p.workers / p.sk_iters);
@@ -496,119 +502,136 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            // Slots are filled kKPerStage at a time: group q holds slots
-            // q*kKPerStage.. and one full/empty barrier pair; a work item's
-            // last group may hold fewer K-blocks.
-            constexpr int GROUPS = STAGES / kKPerStage;
-            int grp = 0;
-            uint32_t phase = 0;
-            uint32_t armed = 0, armed_parity = 0;
-            long long g = 0;
-            bool ok = true;
-            // bytes this CTA lands per K-block (A half + its B columns)
-            const uint32_t a_bytes = TS::kAStage;
-            const uint32_t b_bytes = p.q_mn_major ? (uint32_t)TS::kBStage : (uint32_t)TS::kBNC * 128u;
-            const uint32_t stage_tx = (a_bytes + b_bytes) * (PAIR ? 2u : 1u);
-            const bool both_2k = p.p_2k && p.q_2k;  // both operands have two-K-block maps
-            WorkIter items(p, worker);
-            int t, kb0, kb1;
-            while (ok && items.next(t, kb0, kb1)) {
-                int tm, tn;
-                tile_coords(p, t, tm, tn);
-                const int m0 = tm * TS::kBM + (int)rank * 128;
-                const int n0 = tn * BN + (int)rank * TS::kBNC;
-                for (int kb = kb0; kb < kb1; kb += kKPerStage) {
-                    const int n = kb1 - kb < kKPerStage ? kb1 - kb : kKPerStage;
-                    if (!wait_bar(smem_addr(&empty[grp]), phase ^ 1, w, DEV_TIMEOUT_PRODUCER)) {
-                        ok = false;
-                        break;
+    // ------------------------------------------------------ TMA producers
+    // Two threads fill the ring: role 1 (warp 0) arms each barrier
+    // transaction with both operands' bytes and loads P (A); role 2 (warp
+    // kHelper0, idle until the last tile's epilogue) loads Q (B) into the same
+    // transaction.  A Q load may complete before the transaction is armed: the
+    // phase cannot complete while the arming arrival is pending.  The single
+    // producer thread's loop was on the critical path of the main loop.
+    auto run_producer = [&](auto role) {
+        constexpr int ROLE = decltype(role)::value;
+        // Slots are filled kKPerStage at a time: group q holds slots
+        // q*kKPerStage.. and one full/empty barrier pair; a work item's last
+        // group may hold fewer K-blocks.
+        constexpr int GROUPS = STAGES / kKPerStage;
+        int grp = 0;
+        uint32_t phase = 0;
+        uint32_t armed = 0, armed_parity = 0;
+        long long g = 0;
+        bool ok = true;
+        // bytes this CTA lands per K-block (A half + its B columns)
+        const uint32_t a_bytes = TS::kAStage;
+        const uint32_t b_bytes = p.q_mn_major ? (uint32_t)TS::kBStage : (uint32_t)TS::kBNC * 128u;
+        const uint32_t stage_tx = (a_bytes + b_bytes) * (PAIR ? 2u : 1u);
+        const bool both_2k = p.p_2k && p.q_2k;  // both operands have two-K-block maps
+        WorkIter items(p, worker);
+        int t, kb0, kb1;
+        while (ok && items.next(t, kb0, kb1)) {
+            int tm, tn;
+            tile_coords(p, t, tm, tn);
+            const int m0 = tm * TS::kBM + (int)rank * 128;
+            const int n0 = tn * BN + (int)rank * TS::kBNC;
+            for (int kb = kb0; kb < kb1; kb += kKPerStage) {
+                const int n = kb1 - kb < kKPerStage ? kb1 - kb : kKPerStage;
+                if (!wait_bar(smem_addr(&empty[grp]), phase ^ 1, w, DEV_TIMEOUT_PRODUCER)) {
+                    ok = false;
+                    break;
+                }
+                if (p.inject_skip_load < g || p.inject_skip_load >= g + n) {
+                    const uint32_t fb_local = smem_addr(&full[grp]);
+                    if (ROLE == 1 && leader) {
+                        mbar_arrive_expect_tx(fb_local, stage_tx * (uint32_t)n);
+                        armed |= 1u << grp;
+                        armed_parity = (armed_parity & ~(1u << grp)) | (phase << grp);
                     }
-                    if (p.inject_skip_load < g || p.inject_skip_load >= g + n) {
-                        const uint32_t fb_local = smem_addr(&full[grp]);
-                        if (leader) {
-                            mbar_arrive_expect_tx(fb_local, stage_tx * (uint32_t)n);
-                            armed |= 1u << grp;
-                            armed_parity = (armed_parity & ~(1u << grp)) | (phase << grp);
-                        }
-                        const uint32_t fb = PAIR ? mapa_shared(fb_local, 0) : fb_local;
-                        if (kKPerStage == 2 && n == 2 && both_2k) {
-                            // both K-blocks of each operand as one box
-                            const uint32_t a_dst = smem_addr(sA + grp * kKPerStage * TS::kAStage);
-                            const uint32_t b_dst = smem_addr(sB + grp * kKPerStage * TS::kBStage);
-                            if constexpr (PAIR) {
+                    const uint32_t fb = PAIR ? mapa_shared(fb_local, 0) : fb_local;
+                    if (kKPerStage == 2 && n == 2 && both_2k) {
+                        // both K-blocks of each operand as one box
+                        const uint32_t a_dst = smem_addr(sA + grp * kKPerStage * TS::kAStage);
+                        const uint32_t b_dst = smem_addr(sB + grp * kKPerStage * TS::kBStage);
+                        if constexpr (ROLE == 1) {
+                            if constexpr (PAIR)
                                 tma_load_3d_pair(a_dst, &p.map_p2, fb, 0, m0, kb);
-                                tma_load_4d_pair(b_dst, &p.map_q2, fb, 0, 0, n0 >> 6, kb);
-                            } else {
+                            else
                                 tma_load_3d(a_dst, &p.map_p2, fb, 0, m0, kb);
-                                tma_load_4d(b_dst, &p.map_q2, fb, 0, 0, n0 >> 6, kb);
-                            }
                         } else {
+                            if constexpr (PAIR)
+                                tma_load_4d_pair(b_dst, &p.map_q2, fb, 0, 0, n0 >> 6, kb);
+                            else
+                                tma_load_4d(b_dst, &p.map_q2, fb, 0, 0, n0 >> 6, kb);
+                        }
+                    } else {
 #pragma unroll
-                            for (int j = 0; j < kKPerStage; ++j) {
-                                if (j >= n) break;
-                                const int slot = grp * kKPerStage + j;
-                                const uint32_t a_dst = smem_addr(sA + slot * TS::kAStage);
-                                const uint32_t b_dst = smem_addr(sB + slot * TS::kBStage);
-                                const int k0 = (kb + j) * kBK;
-                                if (p.p_3d) {
-                                    if constexpr (PAIR)
-                                        tma_load_3d_pair(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
-                                    else
-                                        tma_load_3d(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
-                                } else if (p.p_mn_major) {
+                        for (int j = 0; j < kKPerStage; ++j) {
+                            if (j >= n) break;
+                            const int slot = grp * kKPerStage + j;
+                            const uint32_t a_dst = smem_addr(sA + slot * TS::kAStage);
+                            const uint32_t b_dst = smem_addr(sB + slot * TS::kBStage);
+                            const int k0 = (kb + j) * kBK;
+                            if constexpr (ROLE == 1) {
+                            if (p.p_3d) {
+                                if constexpr (PAIR)
+                                    tma_load_3d_pair(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
+                                else
+                                    tma_load_3d(a_dst, &p.map_p, fb, 0, k0, m0 >> 6);
+                            } else if (p.p_mn_major) {
 #pragma unroll
-                                    for (int h = 0; h < 2; ++h) {
-                                        if constexpr (PAIR)
-                                            tma_load_2d_pair(a_dst + h * 8192, &p.map_p, fb, m0 + 64 * h, k0);
-                                        else
-                                            tma_load_2d(a_dst + h * 8192, &p.map_p, fb, m0 + 64 * h, k0);
-                                    }
-                                } else {
+                                for (int h = 0; h < 2; ++h) {
                                     if constexpr (PAIR)
-                                        tma_load_2d_pair(a_dst, &p.map_p, fb, k0, m0);
+                                        tma_load_2d_pair(a_dst + h * 8192, &p.map_p, fb, m0 + 64 * h, k0);
                                     else
-                                        tma_load_2d(a_dst, &p.map_p, fb, k0, m0);
+                                        tma_load_2d(a_dst + h * 8192, &p.map_p, fb, m0 + 64 * h, k0);
                                 }
-                                if (p.q_3d) {
-                                    if constexpr (PAIR)
-                                        tma_load_3d_pair(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
-                                    else
-                                        tma_load_3d(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
-                                } else if (p.q_mn_major) {
+                            } else {
+                                if constexpr (PAIR)
+                                    tma_load_2d_pair(a_dst, &p.map_p, fb, k0, m0);
+                                else
+                                    tma_load_2d(a_dst, &p.map_p, fb, k0, m0);
+                            }
+                            } else {
+                            if (p.q_3d) {
+                                if constexpr (PAIR)
+                                    tma_load_3d_pair(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
+                                else
+                                    tma_load_3d(b_dst, &p.map_q, fb, 0, k0, n0 >> 6);
+                            } else if (p.q_mn_major) {
 #pragma unroll
-                                    for (int h = 0; h < TS::kBBoxes; ++h) {
-                                        if constexpr (PAIR)
-                                            tma_load_2d_pair(b_dst + h * 8192, &p.map_q, fb, n0 + 64 * h, k0);
-                                        else
-                                            tma_load_2d(b_dst + h * 8192, &p.map_q, fb, n0 + 64 * h, k0);
-                                    }
-                                } else {
+                                for (int h = 0; h < TS::kBBoxes; ++h) {
                                     if constexpr (PAIR)
-                                        tma_load_2d_pair(b_dst, &p.map_q, fb, k0, n0);
+                                        tma_load_2d_pair(b_dst + h * 8192, &p.map_q, fb, n0 + 64 * h, k0);
                                     else
-                                        tma_load_2d(b_dst, &p.map_q, fb, k0, n0);
+                                        tma_load_2d(b_dst + h * 8192, &p.map_q, fb, n0 + 64 * h, k0);
                                 }
+                            } else {
+                                if constexpr (PAIR)
+                                    tma_load_2d_pair(b_dst, &p.map_q, fb, k0, n0);
+                                else
+                                    tma_load_2d(b_dst, &p.map_q, fb, k0, n0);
+                            }
                             }
                         }
-                    }
-                    g += n;
-                    if (++grp == GROUPS) {
-                        grp = 0;
-                        phase ^= 1;
                     }
                 }
-            }
-            if (*abort_flag) {
-                // No TMA write may land after the CTA exits: wait for the last
-                // armed phase of every group (the leader's barriers count the
-                // bytes of both CTAs).
-                for (int q = 0; q < GROUPS; ++q)
-                    if (armed & (1u << q)) drain_bar(smem_addr(&full[q]), (armed_parity >> q) & 1, w);
+                g += n;
+                if (++grp == GROUPS) {
+                    grp = 0;
+                    phase ^= 1;
+                }
             }
         }
+        if (*abort_flag) {
+            // No TMA write may land after the CTA exits: wait for the last
+            // armed phase of every group (the leader's barriers count the
+            // bytes of both CTAs).
+            for (int q = 0; q < GROUPS; ++q)
+                if (armed & (1u << q)) drain_bar(smem_addr(&full[q]), (armed_parity >> q) & 1, w);
+        }
+    };
+    if (warp == 0 && lane == 0) {
+        run_producer(RoleTag<1>{});
+    } else if (warp == kHelper0 && lane == 0) {
+        run_producer(RoleTag<2>{});
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer
@@ -704,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // complete.  Helpers meet the main warps at no named barrier: they learn
     // a split tile's fix-up decision through the mbarrier `hsync`, with
     // bounded waits, so an aborting CTA cannot strand them.
-    __syncwarp();  // the lanes of warps 0 and 1 wait for their role's lane 0
+    __syncwarp();  // the lanes of warps 0, 1 and kHelper0 wait for their role's lane 0
     {
         const bool helper = warp < 2 || warp >= kHelper0;
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
@@ -999,14 +1022,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
     tc_fence_before();
     __syncwarp();
-    if constexpr (PAIR) {
-        if (*abort_flag) {
-            // the peer's loads for phases the leader never armed cannot be
-            // observed here: give any such copy ample time to land
-            const long long t0 = clock64();
-            while (clock64() - t0 < 2000000) {
-            }
+    if (*abort_flag) {
+        // loads for phases that were never armed (the peer's, or the second
+        // producer's) cannot be observed here: give any such copy ample time
+        // to land
+        const long long t0 = clock64();
+        while (clock64() - t0 < 2000000) {
         }
+    }
+    if constexpr (PAIR) {
         cluster_sync();  // no CTA leaves while its peer may still signal it
     } else {
         __syncthreads();
