@@ -58,7 +58,7 @@ struct KBlocksPerStage {
 };
 constexpr int kUmmaK = 16;     // K per tcgen05.mma of kind::f16
 constexpr int kEpiWarps = 4;   // one epilogue warp per TMEM lane quadrant (8 measured no faster overall)
-constexpr int kHelper0 = 2 + kEpiWarps;       // first of two warps that only help with a last item
+constexpr int kHelper0 = 2 + kEpiWarps;       // second producer (B loads), then a helper with a last item
 constexpr int kThreads = 64 + 32 * kEpiWarps + 64;  // producer, MMA, epilogue and helper warps
 constexpr int kStageBufs = 4;  // output staging buffers per epilogue warp
 
@@ -720,8 +720,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // Warps 2 .. 1 + kEpiWarps finish every work item, one per TMEM lane
     // quadrant.  Nothing overlaps the epilogue of a worker's last item, so
     // that one is split with a second warp per quadrant (a "helper"): warps
-    // 0 and 1 once their producer / MMA role is done, and warps kHelper0 and
-    // kHelper0 + 1, which wait for it from the start.  A helper takes the
+    // 0, 1 and kHelper0 once their producer / MMA roles are done, and warp
+    // kHelper0 + 1, which waits for it from the start.  A helper takes the
     // second half of its quadrant's chunks and stages them in the operand
     // ring, which no load or MMA touches once the last accumulator is
     // complete.  Helpers meet the main warps at no named barrier: they learn
