@@ -45,16 +45,19 @@
 namespace tg {
 
 constexpr int kBK = 64;        // K elements per ring slot: one 128-byte swizzle row of fp16/bf16
-// K-blocks per barrier transaction in whole-tile kernels: two consecutive
-// ring slots fill and drain together under one full/empty barrier pair.  Each
-// transaction has a fixed cost beside its bytes (a bare TMA stream of 64 KB
-// transactions measured 64.8 B/clk per SM where 32 KB ones reached 39.6), and
-// pairs measured +2.5 % at 8192 x 8192 x 4096.  Stream-K kernels keep one
-// K-block per transaction: their K-ranges start and end anywhere, and pairs
-// measured 1-2 % slower there.
-template <bool SK>
+// K-blocks per barrier transaction: in whole-tile kernels with tiles wider
+// than 64 columns two consecutive ring slots fill and drain together under
+// one full/empty barrier pair.  Each transaction has a fixed cost beside its
+// bytes (a bare TMA stream of 64 KB transactions measured 64.8 B/clk per SM
+// where 32 KB ones reached 39.6): pairs measured +2.5 % at 8192 x 8192 x 4096
+// with one producer thread, and still +0.7 % on the fused GEMM with two.
+// Stream-K kernels keep one K-block per transaction (pairs measured 2.5-4 %
+// slower there with two producer threads), and so do tiles of 32 or 64
+// columns, whose stages are small: the bandwidth-bound 32 x 16384 x 16384
+// measured 1.5 % faster with one.
+template <bool SK, int BN>
 struct KBlocksPerStage {
-    static constexpr int value = SK ? 1 : 2;
+    static constexpr int value = (SK || BN <= 64) ? 1 : 2;
 };
 constexpr int kUmmaK = 16;     // K per tcgen05.mma of kind::f16
 constexpr int kEpiWarps = 4;   // one epilogue warp per TMEM lane quadrant (8 measured no faster overall)
@@ -441,7 +444,7 @@ template <int BN, bool PAIR, bool AUX, bool SK>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
     using TS = TileShape<BN, PAIR>;
     constexpr int STAGES = TS::kStages;
-    constexpr int kKPerStage = KBlocksPerStage<SK>::value;
+    constexpr int kKPerStage = KBlocksPerStage<SK, BN>::value;
     constexpr int CG = PAIR ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128B-swizzle atoms (same offset in both CTAs of a pair)
