@@ -247,19 +247,22 @@ __device__ __forceinline__ bool prefetch_aux(const GemmParams& p, int m, int c0,
 // Epilogue arithmetic for the run C(m, c0 .. c0+31) held in y[], in fp32:
 // scale, bias, ReLU, residual.  Called by all 32 lanes of a warp together
 // (lane = row): lane j holds in `bias_lane` the bias of column c0 + j (0
-// outside C), which shuffles hand to every row.  `a` holds the prefetched
-// residual of a full in-bounds run; otherwise (edge runs) it is loaded here
-// with per-element masks.  Values outside C are computed but never stored.
+// outside C), which shuffles hand to every row; `add_bias` is false where
+// the caller holds no bias (the plain epilogue: no bias step compiled in).
+// `a` holds the prefetched residual of a full in-bounds run; otherwise (edge
+// runs) it is loaded here with per-element masks.  Values outside C are
+// computed but never stored.
 template <bool BF>
 __device__ __forceinline__ void epilogue_math(const GemmParams& p, int m, int c0, float (&y)[32],
-                                              float row_scale, float bias_lane, const Aux* a) {
+                                              float row_scale, float bias_lane, bool add_bias,
+                                              const Aux* a) {
     const bool inside = m < p.M && c0 < p.N;
     const bool full = inside && c0 + 32 <= p.N;
     if (p.scale_m) {
 #pragma unroll
         for (int j = 0; j < 32; j += 2) mul2(y + j, row_scale);
     }
-    if (p.bias_n) {
+    if (p.bias_n && add_bias) {
 #pragma unroll
         for (int j = 0; j < 32; j += 2)
             add2(y + j, __shfl_sync(0xffffffffu, bias_lane, j), __shfl_sync(0xffffffffu, bias_lane, j + 1));
@@ -334,12 +337,13 @@ __device__ __forceinline__ void store_chunk(const GemmParams& p, uint8_t* stage,
 // resolved once per chunk (instead of per element).
 __device__ __forceinline__ void finish_chunk(const GemmParams& p, uint8_t* stage, uint32_t& count,
                                              int lane, int rk, int row0, int c0, float (&y)[32],
-                                             float row_scale, float bias_lane, const Aux* a) {
+                                             float row_scale, float bias_lane, bool add_bias,
+                                             const Aux* a) {
     if (p.bf16) {
-        epilogue_math<true>(p, rk, c0, y, row_scale, bias_lane, a);
+        epilogue_math<true>(p, rk, c0, y, row_scale, bias_lane, add_bias, a);
         store_chunk<true>(p, stage, count, lane, row0, c0, y);
     } else {
-        epilogue_math<false>(p, rk, c0, y, row_scale, bias_lane, a);
+        epilogue_math<false>(p, rk, c0, y, row_scale, bias_lane, add_bias, a);
         store_chunk<false>(p, stage, count, lane, row0, c0, y);
     }
 }
@@ -976,7 +980,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         epilogue_swap(p, rk, tn * BN + c * 32, y, row_bias);
                     } else {
                         finish_chunk(p, stage, chunks, lane, rk, row0, tn * BN + c * 32, y, row_scale,
-                                     pick(bcol, c), nullptr);
+                                     pick(bcol, c), true, nullptr);
                     }
                 }
                 if (warp == 2 && lane == 0) *counter = 0;  // ready for the next call
@@ -1011,12 +1015,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     if (c + 1 < ce)
                         nxt_full = prefetch_aux(p, rk, tn * BN + (c + 1) * 32, nxt, pol);
                     finish_chunk(p, stage, chunks, lane, rk, row0, tn * BN + c * 32, y, row_scale,
-                                 pick(bcol, c), cur_full ? &cur : nullptr);
+                                 pick(bcol, c), true, cur_full ? &cur : nullptr);
                     cur = nxt;
                     cur_full = nxt_full;
                 } else {
                     finish_chunk(p, stage, chunks, lane, rk, row0, tn * BN + c * 32, y, row_scale,
-                                 0.0f, nullptr);
+                                 0.0f, false, nullptr);
                 }
             }
         }
