@@ -22,6 +22,7 @@ import glob
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -46,16 +47,26 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the sources that define the GEMM kernel, its launch and its
-    tile selection (not the host layout module or the probes)."""
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source text with its comments removed and its whitespace
+    collapsed (the sources hold no comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_source_hash(csrc: str | None = None) -> str:
+    """Hash of the code that defines the GEMM kernel, its launch and its tile
+    selection (not the host layout module or the probes).  Comments and
+    whitespace do not count, so a counter capture stays matched to the code
+    it was taken on."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "tiled_gemm_layouts_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "tiled_gemm_layouts_gb300", "csrc")
     files = [f for f in glob.glob(os.path.join(csrc, "*"))
              if os.path.basename(f).startswith(("gemm_", "api.", "select.", "ptx."))]
     for f in sorted(files):
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -5,6 +5,10 @@ multicast TMA copy: every tile a CTA needs is loaded by that CTA (or by its
 pair partner through cta_group::2), so no cp.async.bulk instruction may carry
 a multicast qualifier.  The one multicast in the sources is the tcgen05.commit
 that signals both CTAs of a pair, which is not a copy.
+
+The bench's hash of the kernel code, which ties committed ncu counters to the
+code they were taken on, is checked here too: it ignores comments and
+whitespace and follows every change to the code.
 """
 import os
 import re
@@ -43,3 +47,25 @@ def test_multicast_appears_only_on_the_pair_commit():
     assert hits, "expected the pair commit's multicast qualifier"
     for path, i, line in hits:
         assert "tcgen05.commit" in line, f"{path}:{i}: {line.strip()}"
+
+
+def test_kernel_hash_follows_code_not_comments(tmp_path):
+    # bench.py matches committed ncu counters to the kernel code by this hash:
+    # comment and whitespace edits keep it, any change to the code moves it
+    import shutil
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    src = os.path.join(tmp_path, "csrc")
+    shutil.copytree(CSRC, src)
+    base = bench.kernel_source_hash(src)
+    assert base == bench.kernel_source_hash()
+    k = os.path.join(src, "gemm_kernel.cuh")
+    text = open(k).read()
+    with open(k, "w") as f:
+        f.write("/* a block\n   comment */\n" + text.replace("\n", "\n\n", 3) + "\n// trailing note\n")
+    assert bench.kernel_source_hash(src) == base
+    assert "constexpr int kStageBufs = 4;" in text
+    with open(k, "w") as f:
+        f.write(text.replace("constexpr int kStageBufs = 4;", "constexpr int kStageBufs = 3;"))
+    assert bench.kernel_source_hash(src) != base

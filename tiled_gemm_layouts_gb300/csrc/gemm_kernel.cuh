@@ -7,9 +7,11 @@
 // (row scale, column bias, ReLU, residual) and is stored in the input dtype.
 //
 // GB300 mapping (one CTA per SM, persistent over output tiles):
-//   warp 0      TMA producer: fills an S-stage ring of 128B-swizzled shared
-//               tiles, one mbarrier "full"/"empty" pair per stage.  Tails of
-//               M, N and K are zero-filled by the tensor map, so they add 0.
+//   warp 0      TMA producer of A: fills an S-slot ring of 128B-swizzled
+//               shared tiles and arms each barrier transaction (one mbarrier
+//               "full"/"empty" pair per group of slots).  Tails of M, N and K
+//               are zero-filled by the tensor map, so they add 0.
+//   warp 6      TMA producer of B into the same transactions.
 //   warp 1      owns TMEM; one thread issues tcgen05.mma (K=16 per
 //               instruction) into a double-buffered fp32 accumulator.
 //   warps 2..5  epilogue: tcgen05.ld 32x32b (thread t of warp w holds TMEM
@@ -19,6 +21,8 @@
 //               (rows past M and columns past N clipped by the tensor map; a
 //               ragged last few columns stored directly), while the next
 //               tile's main loop already runs in the other accumulator buffer.
+//   warps 0, 1, 6 (once their roles end) and 7 take half of the chunks of a
+//               worker's last tile, whose epilogue nothing else overlaps.
 // SK = true adds the stream-K tail: tiles of the last, part-empty wave are
 // cut into K-ranges dealt out to every worker; contributors publish fp32
 // partial sums to a caller workspace and the last to arrive adds them and
